@@ -1,0 +1,235 @@
+/*
+ * moe_route.h - C ABI of the GB300 (sm_103a) MoE token-routing library
+ * (libmoe_route.so).
+ *
+ * The library implements the data-parallel routing path of a
+ * MegaBlocks-style Mixture-of-Experts layer:
+ *   route build -> binned / padded gather (permute) -> [expert FFN, not here]
+ *   -> binned / padded scatter (combine) -> router-weight gradient,
+ * plus the dense routing-map -> fixed-width top-k compaction and its
+ * backward. Sources, by page title and section:
+ *   [binned] "Build Triton-Ascend Binned MoE Routing": Goal, Workflow,
+ *            Implementation Pattern, Ascend Guardrails, Verification.
+ *   [padded] "Build Triton-Ascend Padded MoE Routing": Goal, Workflow,
+ *            Implementation Pattern, Ascend Guardrails, Verification.
+ *   [mok]    Megatron-Core API docs, core.transformer.moe.megakernel.mok.
+ *            route_adapter: RoutingMapToIndices, routing_map_to_mok_inputs.
+ *
+ * Conventions (all entry points):
+ *  - Every pointer is a DEVICE pointer owned by the caller. The library
+ *    allocates no memory: scratch space is passed in through `workspace`,
+ *    sized by the matching *_workspace_size() call.
+ *  - Work is enqueued on `stream` (a cudaStream_t; NULL = the legacy default
+ *    stream) and runs asynchronously. No entry point synchronises the host.
+ *  - Outputs are written completely, zeros included; callers need not clear
+ *    them. Inputs are read-only. Outputs must not alias inputs or each other.
+ *  - Assignment id a = t * top_k + k for token t and slot k; n = T * top_k.
+ *    Index vectors are int32 and n must fit in int32.
+ *  - dtype selects the activation type: MOE_F32 (float) or MOE_BF16
+ *    (__nv_bfloat16 bits). Router weights, wgrad and all compaction floats
+ *    are fp32. Activations are row-major [rows, hidden].
+ *  - Return value: MOE_OK, or an MOE_ERR_* code. Argument errors are found
+ *    on the host before anything is enqueued; MOE_ERR_CUDA reports a launch
+ *    failure (cudaGetLastError).
+ *  - Errors in device-resident data (an expert id outside [0, E), bins that
+ *    are not monotonic, an index outside its range) cannot be reported
+ *    synchronously. Entry points that read such data take `d_status`: a
+ *    nullable device int32 into which kernels OR MOE_STATUS_* bits. Kernels
+ *    never trap; they skip the offending element, keep every access in
+ *    bounds, and leave the affected outputs unspecified. The caller clears
+ *    *d_status before the calls it wants to check.
+ */
+#ifndef MOE_ROUTE_H
+#define MOE_ROUTE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t. */
+typedef struct CUstream_st* moe_stream_t;
+
+enum moe_error {
+  MOE_OK = 0,
+  MOE_ERR_INVALID_ARG = 1, /* null required pointer, size out of range, n overflowing int32 */
+  MOE_ERR_UNSUPPORTED = 2, /* dtype, or a pointer not aligned to its element size */
+  MOE_ERR_CUDA = 3         /* a kernel launch failed */
+};
+
+enum moe_dtype { MOE_F32 = 0, MOE_BF16 = 1 };
+
+/* Bits OR-ed into *d_status by kernels that meet invalid device data. */
+enum moe_device_status {
+  MOE_STATUS_BAD_EXPERT = 1,   /* expert id outside [0, E) */
+  MOE_STATUS_BAD_INDEX = 2,    /* an index or position outside its range */
+  MOE_STATUS_BAD_BINS = 4,     /* bins / padded_bins not monotonic or not consistent */
+  MOE_STATUS_ROWS_MISMATCH = 8 /* padded_bins[E-1] exceeds the rows the caller provided */
+};
+
+/* Library limits (inclusive). */
+#define MOE_MAX_EXPERTS 4096
+#define MOE_MAX_TOP_K 64
+
+/* Human-readable name of an MOE_ERR_* code (static string). */
+const char* moe_error_string(int code);
+
+/* Library version as major*10000 + minor*100 + patch. */
+int moe_version(void);
+
+/*
+ * Route build ([padded] Workflow steps 1-3; [binned] Workflow steps 1-2).
+ * Stable counting sort of the n = T*top_k expert choices by expert id.
+ *   top_expert  [n] int32   expert of assignment a (row-major [T, top_k]).
+ *   indices     [n] int32   out: assignment id at each sorted position;
+ *                           within an expert, ids ascend (stable).
+ *   bin_ids     [n] int32   out: expert of each sorted position
+ *                           (nondecreasing).
+ *   bins        [E] int32   out: inclusive cumulative count through expert e
+ *                           (bins[E-1] == n).
+ *   padded_bins [E] int32   out, nullable: inclusive cumulative sum of each
+ *                           count rounded up to a multiple of pad_multiple
+ *                           (an empty expert stays 0 rows).
+ *   positions   [n] int32   out, nullable: inverse of indices
+ *                           (positions[indices[i]] == i). Passing it to the
+ *                           scatter entry points saves them a pass.
+ *   workspace   >= moe_route_build_workspace_size(n, E) bytes of device
+ *                           scratch, 4-byte aligned; contents need no
+ *                           initialisation and are clobbered.
+ * Requires 0 <= n <= INT32_MAX, 1 <= E <= MOE_MAX_EXPERTS, pad_multiple >= 1
+ * and n + E*(pad_multiple-1) <= INT32_MAX. An expert id outside [0, E) sets
+ * MOE_STATUS_BAD_EXPERT and is left out of every output (outputs are then
+ * unspecified).
+ */
+size_t moe_route_build_workspace_size(int64_t n, int32_t num_experts);
+int moe_route_build(const int32_t* top_expert, int64_t n, int32_t num_experts,
+                    int32_t pad_multiple, int32_t* indices, int32_t* bin_ids,
+                    int32_t* bins, int32_t* padded_bins, int32_t* positions,
+                    void* workspace, size_t workspace_bytes, int32_t* d_status,
+                    moe_stream_t stream);
+
+/*
+ * Binned gather ([binned] Goal, Workflow step 3, Implementation Pattern,
+ * Guardrails). For expert e and slot j < capacity:
+ *   out[e, j, :] = x[indices[bins[e-1] + j] / top_k, :]  if j < count_e,
+ *                  0                                      otherwise,
+ * with bins[-1] read as 0. Assignments beyond capacity are dropped.
+ *   x    [T, H] dtype;  out [E, capacity, H] dtype (fully written).
+ *   indices [n], bins [E] from moe_route_build; n = T*top_k.
+ * capacity >= 0; capacity == 0 writes nothing.
+ */
+int moe_binned_gather(const void* x, int32_t dtype, const int32_t* indices,
+                      const int32_t* bins, int64_t num_tokens, int64_t hidden,
+                      int32_t num_experts, int32_t capacity, int32_t top_k,
+                      void* out, int32_t* d_status, moe_stream_t stream);
+
+/*
+ * Padded gather ([padded] Goal, Workflow steps 4-5, Implementation Pattern,
+ * Guardrails). Row padded_bins[e-1] + j of out receives
+ * x[indices[bins[e-1] + j] / top_k] for j < count_e; padding rows are zero.
+ *   out [out_rows, H] dtype. out_rows is the caller's row count, normally
+ *   padded_bins[E-1] (read back by the caller to size the buffer). Rows at
+ *   or beyond padded_bins[E-1] are zero-filled; if padded_bins[E-1] exceeds
+ *   out_rows, rows past out_rows are not written and MOE_STATUS_ROWS_MISMATCH
+ *   is set.
+ */
+int moe_padded_gather(const void* x, int32_t dtype, const int32_t* indices,
+                      const int32_t* bins, const int32_t* padded_bins,
+                      int64_t num_tokens, int64_t hidden, int32_t num_experts,
+                      int32_t top_k, void* out, int64_t out_rows,
+                      int32_t* d_status, moe_stream_t stream);
+
+/*
+ * Scatter / combine ([binned] Workflow step 5, Guardrails; [padded]
+ * Workflow step 6, Guardrails). For each token t:
+ *   out[t, :] = sum_{k=0..top_k-1, slot kept} s_a * xe[row(a), :],
+ *   a = t*top_k + k, s_a = weights[a] (or 1 when weights == NULL),
+ * accumulated in fp32 in increasing k starting from +0.0, each weighted
+ * term rounded as fl(s_a * v) (no fused multiply-add), then rounded to
+ * dtype (nearest even). A slot is kept when its offset in its expert is
+ * below capacity (binned) or always (padded); dropped slots add nothing,
+ * so a token whose slots are all dropped gets +0.0.
+ *   xe  [E, capacity, H] (binned) or [xe_rows, H] (padded), dtype;
+ *   out [T, H] dtype; weights [n] fp32 nullable, indexed by assignment id.
+ *   positions [n] nullable: the inverse permutation from moe_route_build.
+ *   When NULL it is rebuilt in `workspace`
+ *   (>= moe_scatter_workspace_size(n) bytes); otherwise workspace may be
+ *   NULL.
+ */
+size_t moe_scatter_workspace_size(int64_t n);
+int moe_binned_scatter(const void* xe, int32_t dtype, const int32_t* indices,
+                       const int32_t* bin_ids, const int32_t* bins,
+                       const float* weights, const int32_t* positions,
+                       int64_t num_tokens, int64_t hidden, int32_t num_experts,
+                       int32_t capacity, int32_t top_k, void* out,
+                       void* workspace, size_t workspace_bytes,
+                       int32_t* d_status, moe_stream_t stream);
+int moe_padded_scatter(const void* xe, int32_t dtype, const int32_t* indices,
+                       const int32_t* bin_ids, const int32_t* bins,
+                       const int32_t* padded_bins, const float* weights,
+                       const int32_t* positions, int64_t num_tokens,
+                       int64_t hidden, int32_t num_experts, int32_t top_k,
+                       int64_t xe_rows, void* out, void* workspace,
+                       size_t workspace_bytes, int32_t* d_status,
+                       moe_stream_t stream);
+
+/*
+ * Router-weight gradient ([binned] Workflow step 6, Guardrails; [padded]
+ * Workflow step 6, Guardrails). For every sorted position i with
+ * assignment a = indices[i]:
+ *   wgrad[a] = dot(xe[row(i), :], grad[a / top_k, :])  if i is kept,
+ *              0                                        otherwise.
+ * Accumulated in fp32 with compensated (error-free transformation)
+ * summation, so the result is close to the correctly rounded dot.
+ *   xe as for scatter; grad [T, H] dtype; wgrad [n] fp32 (fully written).
+ */
+int moe_binned_wgrad(const void* xe, const void* grad, int32_t dtype,
+                     const int32_t* indices, const int32_t* bin_ids,
+                     const int32_t* bins, int64_t num_tokens, int64_t hidden,
+                     int32_t num_experts, int32_t capacity, int32_t top_k,
+                     float* wgrad, int32_t* d_status, moe_stream_t stream);
+int moe_padded_wgrad(const void* xe, const void* grad, int32_t dtype,
+                     const int32_t* indices, const int32_t* bin_ids,
+                     const int32_t* bins, const int32_t* padded_bins,
+                     int64_t num_tokens, int64_t hidden, int32_t num_experts,
+                     int32_t top_k, int64_t xe_rows, float* wgrad,
+                     int32_t* d_status, moe_stream_t stream);
+
+/*
+ * Dense routing map -> fixed-width compaction ([mok] RoutingMapToIndices,
+ * forward; routing_map_to_mok_inputs). Row t lists the experts e with
+ * routing_map[t, e] != 0 in increasing e; the first topk of them give
+ *   indices[t, j] = e,  probs_indices[t, j] = probs[t, e];
+ * the remaining slots get -1 and 0.0f. Routes beyond topk are dropped.
+ *   probs [T, E] fp32; routing_map [T, E] int8 (a bool map has the same
+ *   bytes); probs_indices [T, topk] fp32 out; indices [T, topk] int32 out.
+ * T >= 0, E >= 1, topk >= 1 (topk may exceed E: extra slots are padding).
+ */
+int moe_routing_map_to_indices_fwd(const float* probs, const int8_t* routing_map,
+                                   int64_t num_tokens, int32_t num_experts,
+                                   int32_t topk, float* probs_indices,
+                                   int32_t* indices, moe_stream_t stream);
+
+/*
+ * Backward of the compaction ([mok] RoutingMapToIndices, backward):
+ *   grad_probs[t, :] = 0;  grad_probs[t, indices[t, j]] = grad_probs_indices[t, j]
+ * for every slot with indices[t, j] != -1 (the gradient for the integer
+ * indices has no meaning and is not taken). With repeated indices in a row
+ * the highest j wins. An index outside [-1, E) sets MOE_STATUS_BAD_INDEX and
+ * is skipped.
+ *   grad_probs_indices [T, topk] fp32; indices [T, topk] int32;
+ *   grad_probs [T, E] fp32 out (fully written).
+ */
+int moe_routing_map_to_indices_bwd(const float* grad_probs_indices,
+                                   const int32_t* indices, int64_t num_tokens,
+                                   int32_t num_experts, int32_t topk,
+                                   float* grad_probs, int32_t* d_status,
+                                   moe_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOE_ROUTE_H */

@@ -1,0 +1,17 @@
+"""GB300-native MoE token routing: route build, binned / padded gather
+(permute), scatter (combine), router-weight gradient and the dense
+routing-map compaction, as hand-written sm_103a CUDA kernels behind the C ABI
+in include/moe_route.h, with a thin Python binding of the same names."""
+from ._lib import MoeError, load  # noqa: F401
+from .ops import (  # noqa: F401
+    Route,
+    moe_binned_gather,
+    moe_binned_scatter,
+    moe_binned_wgrad,
+    moe_padded_gather,
+    moe_padded_scatter,
+    moe_padded_wgrad,
+    moe_route_build,
+    moe_routing_map_to_indices_bwd,
+    moe_routing_map_to_indices_fwd,
+)

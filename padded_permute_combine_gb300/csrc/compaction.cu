@@ -1,0 +1,148 @@
+// Dense routing map -> fixed-width top-k compaction, and its backward
+// (Megatron-Core API docs, core.transformer.moe.megakernel.mok.route_adapter:
+//  RoutingMapToIndices forward / backward, routing_map_to_mok_inputs).
+//
+// Forward: one thread per token row. The row of the int8 map is read in
+// 16-byte vectors; __vcmpne4 turns each word into a nonzero-byte mask, and
+// the set bits are walked in increasing expert order until topk routes are
+// emitted; the rest of the row is padded with -1 / 0.0f.
+// Backward: one thread per group of four dense outputs, so the dense
+// gradient is written with full-width coalesced stores; each thread scans the
+// row's topk compact slots (cached in L1) for indices that fall in its group.
+#include "common.cuh"
+
+namespace moe {
+namespace {
+
+constexpr int kThreads = 256;
+
+// Bit b of the result is set when byte b of w is nonzero.
+__device__ __forceinline__ unsigned nonzero_bytes(uint32_t w) {
+  const uint32_t m = __vcmpne4(w, 0u) & 0x80808080u;
+  return ((m >> 7) | (m >> 14) | (m >> 21) | (m >> 28)) & 0xFu;
+}
+
+template <bool VEC16>
+__global__ void __launch_bounds__(kThreads)
+    compaction_fwd_kernel(const float* __restrict__ probs, const int8_t* __restrict__ rmap, int64_t T, int32_t E,
+                          int32_t topk, float* __restrict__ probs_indices, int32_t* __restrict__ indices) {
+  for (int64_t t = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; t < T; t += (int64_t)gridDim.x * blockDim.x) {
+    const int8_t* row = rmap + t * E;
+    const float* prow = probs + t * E;
+    float* po = probs_indices + t * topk;
+    int32_t* io = indices + t * topk;
+    int j = 0;
+    if (VEC16) {
+      for (int c = 0; c < E && j < topk; c += 16) {
+        const uint4 v = __ldg(reinterpret_cast<const uint4*>(row + c));
+        unsigned mask = nonzero_bytes(v.x) | (nonzero_bytes(v.y) << 4) | (nonzero_bytes(v.z) << 8) |
+                        (nonzero_bytes(v.w) << 12);
+        while (mask != 0u && j < topk) {
+          const int e = c + __ffs(mask) - 1;
+          mask &= mask - 1u;
+          io[j] = e;
+          po[j] = __ldg(prow + e);
+          ++j;
+        }
+      }
+    } else {
+      for (int e = 0; e < E && j < topk; ++e) {
+        if (__ldg(row + e) != 0) {
+          io[j] = e;
+          po[j] = __ldg(prow + e);
+          ++j;
+        }
+      }
+    }
+    for (; j < topk; ++j) {
+      io[j] = -1;
+      po[j] = 0.0f;
+    }
+  }
+}
+
+// G = dense outputs per thread (4 with float4 stores, else 1).
+template <int G>
+__global__ void __launch_bounds__(kThreads)
+    compaction_bwd_kernel(const float* __restrict__ gpi, const int32_t* __restrict__ indices, int64_t T, int32_t E,
+                          int32_t topk, float* __restrict__ grad_probs, int32_t* status) {
+  const int64_t groups_per_row = E / G;
+  const int64_t total = T * groups_per_row;
+  for (int64_t q = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; q < total; q += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t t = q / groups_per_row;
+    const int e0 = (int)(q - t * groups_per_row) * G;
+    float o[G];
+#pragma unroll
+    for (int u = 0; u < G; ++u) o[u] = 0.0f;
+    const int32_t* irow = indices + t * topk;
+    const float* grow = gpi + t * topk;
+    bool bad = false;
+    for (int j = 0; j < topk; ++j) {
+      const int32_t e = __ldg(irow + j);
+      const unsigned d = (unsigned)(e - e0);
+      if (d < (unsigned)G) {
+#pragma unroll
+        for (int u = 0; u < G; ++u)
+          if (d == (unsigned)u) o[u] = __ldg(grow + j);
+      }
+      bad |= (e < -1 || e >= E);
+    }
+    if (bad && e0 == 0) flag_status(status, MOE_STATUS_BAD_INDEX);
+    if (G == 4) {
+      *reinterpret_cast<float4*>(grad_probs + t * E + e0) = make_float4(o[0], o[G > 1 ? 1 : 0], o[G > 2 ? 2 : 0],
+                                                                        o[G > 3 ? 3 : 0]);
+    } else {
+      grad_probs[t * E + e0] = o[0];
+    }
+  }
+}
+
+template <typename K>
+int grid_for(K k, int64_t work) {
+  return persistent_grid(k, kThreads, 0, (work + kThreads - 1) / kThreads);
+}
+
+}  // namespace
+}  // namespace moe
+
+using namespace moe;
+
+extern "C" int moe_routing_map_to_indices_fwd(const float* probs, const int8_t* routing_map, int64_t T, int32_t E,
+                                              int32_t topk, float* probs_indices, int32_t* indices,
+                                              moe_stream_t stream) {
+  if (T < 0 || E < 1 || topk < 1) return MOE_ERR_INVALID_ARG;
+  if (T > 0 && (probs == nullptr || routing_map == nullptr || probs_indices == nullptr || indices == nullptr))
+    return MOE_ERR_INVALID_ARG;
+  if (!aligned(probs, 4) || !aligned(probs_indices, 4) || !aligned(indices, 4)) return MOE_ERR_UNSUPPORTED;
+  if (T == 0) return MOE_OK;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (E % 16 == 0 && aligned(routing_map, 16)) {
+    auto k = compaction_fwd_kernel<true>;
+    k<<<grid_for(k, T), kThreads, 0, s>>>(probs, routing_map, T, E, topk, probs_indices, indices);
+  } else {
+    auto k = compaction_fwd_kernel<false>;
+    k<<<grid_for(k, T), kThreads, 0, s>>>(probs, routing_map, T, E, topk, probs_indices, indices);
+  }
+  return check_launch();
+}
+
+extern "C" int moe_routing_map_to_indices_bwd(const float* grad_probs_indices, const int32_t* indices, int64_t T,
+                                              int32_t E, int32_t topk, float* grad_probs, int32_t* d_status,
+                                              moe_stream_t stream) {
+  if (T < 0 || E < 1 || topk < 1) return MOE_ERR_INVALID_ARG;
+  if (T > 0 && (grad_probs_indices == nullptr || indices == nullptr || grad_probs == nullptr))
+    return MOE_ERR_INVALID_ARG;
+  if (!aligned(grad_probs_indices, 4) || !aligned(indices, 4) || !aligned(grad_probs, 4) ||
+      (d_status && !aligned(d_status, 4)))
+    return MOE_ERR_UNSUPPORTED;
+  if (T == 0) return MOE_OK;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (E % 4 == 0 && aligned(grad_probs, 16)) {
+    auto k = compaction_bwd_kernel<4>;
+    k<<<grid_for(k, T * (E / 4)), kThreads, 0, s>>>(grad_probs_indices, indices, T, E, topk, grad_probs, d_status);
+  } else {
+    auto k = compaction_bwd_kernel<1>;
+    k<<<grid_for(k, T * E), kThreads, 0, s>>>(grad_probs_indices, indices, T, E, topk, grad_probs, d_status);
+  }
+  return check_launch();
+}

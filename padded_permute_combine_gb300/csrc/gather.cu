@@ -1,0 +1,195 @@
+// Binned and padded gather, the "permute" of the MoE layer
+// ("Build Triton-Ascend Binned MoE Routing": Goal, Workflow step 3,
+//  Implementation Pattern, Guardrails;
+//  "Build Triton-Ascend Padded MoE Routing": Goal, Workflow steps 4-5,
+//  Implementation Pattern, Guardrails).
+//
+// Destination-major: every output row is produced exactly once, either as a
+// copy of its source token row or as zeros (unused capacity / padding), so no
+// separate clearing pass is needed. One warp owns one output row at a time
+// and streams it with VB-byte vectors, U vectors per lane in flight. The bin
+// vectors are staged in shared memory; a padded row finds its expert by
+// binary search over padded_bins.
+#include "common.cuh"
+
+namespace moe {
+namespace {
+
+constexpr int kThreads = 256;
+constexpr int kStageMax = 1024;  // experts whose bins are staged in shared memory
+
+struct GatherArgs {
+  const char* x;
+  char* out;
+  const int32_t* indices;
+  const int32_t* bins;
+  const int32_t* padded_bins;  // nullptr: binned
+  int64_t n;
+  int64_t rows_out;
+  int64_t vecs;  // vectors per row
+  int32_t E;
+  int32_t capacity;
+  int32_t top_k;
+  int32_t* status;
+};
+
+// Source token of output row `row`, or -1 for a zero row.
+template <bool PADDED>
+__device__ __forceinline__ int64_t source_token(const GatherArgs& g, const int32_t* sb, const int32_t* spb,
+                                                int64_t row) {
+  int32_t e;
+  int64_t j, seg_len = 0;
+  if (!PADDED) {
+    e = (int32_t)(row / g.capacity);
+    j = row - (int64_t)e * g.capacity;
+  } else {
+    if (row >= spb[g.E - 1]) return -1;  // beyond the last padded segment
+    // first expert whose inclusive padded end exceeds row
+    int lo = 0, hi = g.E - 1;
+    while (lo < hi) {
+      const int mid = (lo + hi) >> 1;
+      if (spb[mid] > row) hi = mid; else lo = mid + 1;
+    }
+    e = lo;
+    const int64_t pstart = e > 0 ? spb[e - 1] : 0;
+    j = row - pstart;
+    seg_len = (int64_t)spb[e] - pstart;
+  }
+  const int64_t start = e > 0 ? sb[e - 1] : 0;
+  const int64_t count = (int64_t)sb[e] - start;
+  if (count < 0 || (PADDED && (count > seg_len || j < 0))) {
+    flag_status(g.status, MOE_STATUS_BAD_BINS);
+    return -1;
+  }
+  if (j >= count) return -1;
+  const int64_t i = start + j;
+  if (i < 0 || i >= g.n) {
+    flag_status(g.status, MOE_STATUS_BAD_BINS);
+    return -1;
+  }
+  const int32_t a = __ldg(g.indices + i);
+  if (a < 0 || a >= g.n) {
+    flag_status(g.status, MOE_STATUS_BAD_INDEX);
+    return -1;
+  }
+  return a / g.top_k;
+}
+
+template <int VB, int U, bool PADDED>
+__global__ void __launch_bounds__(kThreads) gather_kernel(GatherArgs g) {
+  using V = typename Vec<VB>::T;
+  __shared__ int32_t sbins[kStageMax];
+  __shared__ int32_t spbins[PADDED ? kStageMax : 1];
+  const bool staged = g.E <= kStageMax;
+  if (staged) {
+    for (int e = threadIdx.x; e < g.E; e += blockDim.x) {
+      sbins[e] = __ldg(g.bins + e);
+      if (PADDED) spbins[e] = __ldg(g.padded_bins + e);
+    }
+    __syncthreads();
+  }
+  const int32_t* sb = staged ? sbins : g.bins;
+  const int32_t* spb = PADDED ? (staged ? spbins : g.padded_bins) : nullptr;
+  if (PADDED && threadIdx.x == 0 && blockIdx.x == 0 && spb[g.E - 1] > g.rows_out)
+    flag_status(g.status, MOE_STATUS_ROWS_MISMATCH);
+
+  const int lane = lane_id();
+  const int64_t warps = (int64_t)gridDim.x * (blockDim.x / kWarp);
+  const V* __restrict__ x = reinterpret_cast<const V*>(g.x);
+  V* __restrict__ out = reinterpret_cast<V*>(g.out);
+  for (int64_t row = (int64_t)blockIdx.x * (blockDim.x / kWarp) + threadIdx.x / kWarp; row < g.rows_out;
+       row += warps) {
+    const int64_t src = source_token<PADDED>(g, sb, spb, row);
+    V* dst = out + row * g.vecs;
+    if (src >= 0) {
+      const V* s = x + src * g.vecs;
+      for (int64_t c0 = 0; c0 < g.vecs; c0 += kWarp * U) {
+        V v[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+          const int64_t c = c0 + u * kWarp + lane;
+          if (c < g.vecs) v[u] = ld_stream(s + c);
+        }
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+          const int64_t c = c0 + u * kWarp + lane;
+          if (c < g.vecs) st_stream(dst + c, v[u]);
+        }
+      }
+    } else {
+      const V z = zero_vec<V>();
+      for (int64_t c = lane; c < g.vecs; c += kWarp) st_stream(dst + c, z);
+    }
+  }
+}
+
+template <int VB, bool PADDED>
+int launch_gather(const GatherArgs& g, cudaStream_t s) {
+  constexpr int U = VB >= 8 ? 8 : 16;
+  auto k = gather_kernel<VB, U, PADDED>;
+  const int64_t work_ctas = (g.rows_out + (kThreads / kWarp) - 1) / (kThreads / kWarp);
+  const int grid = persistent_grid(k, kThreads, 0, work_ctas);
+  k<<<grid, kThreads, 0, s>>>(g);
+  return check_launch();
+}
+
+template <bool PADDED>
+int dispatch_gather(GatherArgs g, int elem, const void* x, void* out, cudaStream_t s) {
+  const int64_t row_bytes = g.vecs * elem;  // g.vecs holds H on entry
+  const void* ptrs[] = {x, out};
+  const int vb = pick_vec_bytes(row_bytes, ptrs, 2, elem);
+  if (vb == 0) return MOE_ERR_UNSUPPORTED;
+  g.vecs = row_bytes / vb;
+  switch (vb) {
+    case 16: return launch_gather<16, PADDED>(g, s);
+    case 8: return launch_gather<8, PADDED>(g, s);
+    case 4: return launch_gather<4, PADDED>(g, s);
+    default: return launch_gather<2, PADDED>(g, s);
+  }
+}
+
+int gather_checks(const void* x, int32_t dtype, const int32_t* indices, const int32_t* bins, int64_t T, int64_t H,
+                  int32_t E, int32_t top_k, const void* out, int32_t* d_status) {
+  if (dtype_bytes(dtype) == 0) return MOE_ERR_UNSUPPORTED;
+  if (T < 0 || H < 0 || E < 1 || E > MOE_MAX_EXPERTS || top_k < 1 || top_k > MOE_MAX_TOP_K)
+    return MOE_ERR_INVALID_ARG;
+  if (T * top_k > INT32_MAX) return MOE_ERR_INVALID_ARG;
+  if (bins == nullptr || (T > 0 && (x == nullptr || indices == nullptr))) return MOE_ERR_INVALID_ARG;
+  const int eb = dtype_bytes(dtype);
+  if ((x && !aligned(x, eb)) || (out && !aligned(out, eb))) return MOE_ERR_UNSUPPORTED;
+  if (!aligned(indices, 4) || !aligned(bins, 4) || (d_status && !aligned(d_status, 4))) return MOE_ERR_UNSUPPORTED;
+  return MOE_OK;
+}
+
+}  // namespace
+}  // namespace moe
+
+using namespace moe;
+
+extern "C" int moe_binned_gather(const void* x, int32_t dtype, const int32_t* indices, const int32_t* bins,
+                                 int64_t T, int64_t H, int32_t E, int32_t capacity, int32_t top_k, void* out,
+                                 int32_t* d_status, moe_stream_t stream) {
+  const int rc = gather_checks(x, dtype, indices, bins, T, H, E, top_k, out, d_status);
+  if (rc != MOE_OK) return rc;
+  if (capacity < 0) return MOE_ERR_INVALID_ARG;
+  const int64_t rows = (int64_t)E * capacity;
+  if (rows == 0 || H == 0) return MOE_OK;
+  if (out == nullptr) return MOE_ERR_INVALID_ARG;
+  GatherArgs g{static_cast<const char*>(x), static_cast<char*>(out), indices, bins, nullptr, T * top_k, rows, H,
+               E, capacity, top_k, d_status};
+  return dispatch_gather<false>(g, dtype_bytes(dtype), x, out, reinterpret_cast<cudaStream_t>(stream));
+}
+
+extern "C" int moe_padded_gather(const void* x, int32_t dtype, const int32_t* indices, const int32_t* bins,
+                                 const int32_t* padded_bins, int64_t T, int64_t H, int32_t E, int32_t top_k,
+                                 void* out, int64_t out_rows, int32_t* d_status, moe_stream_t stream) {
+  const int rc = gather_checks(x, dtype, indices, bins, T, H, E, top_k, out, d_status);
+  if (rc != MOE_OK) return rc;
+  if (padded_bins == nullptr || out_rows < 0) return MOE_ERR_INVALID_ARG;
+  if (!aligned(padded_bins, 4)) return MOE_ERR_UNSUPPORTED;
+  if (out_rows == 0 || H == 0) return MOE_OK;
+  if (out == nullptr) return MOE_ERR_INVALID_ARG;
+  GatherArgs g{static_cast<const char*>(x), static_cast<char*>(out), indices, bins, padded_bins, T * top_k, out_rows,
+               H, E, 0, top_k, d_status};
+  return dispatch_gather<true>(g, dtype_bytes(dtype), x, out, reinterpret_cast<cudaStream_t>(stream));
+}

@@ -1,0 +1,224 @@
+// Route build: stable counting sort of expert choices by expert id
+// ("Build Triton-Ascend Padded MoE Routing", Workflow steps 1-3;
+//  "Build Triton-Ascend Binned MoE Routing", Workflow steps 1-2).
+//
+// Three launches, no inter-CTA waiting:
+//   1. hist:    CTA g counts the expert ids of its chunk -> counts[g][e].
+//   2. scan:    one CTA turns counts into per-(chunk, expert) start offsets
+//               (exclusive over experts, then over chunks) and writes bins
+//               and padded_bins.
+//   3. scatter: CTA g re-reads its chunk and gives every assignment its
+//               stable rank: warps own consecutive sub-chunks, a warp-level
+//               multi-split (__match_any_sync + popc of lower peers) ranks
+//               lanes within a round, and per-warp running counters in
+//               shared memory carry ranks across rounds and warps.
+#include "common.cuh"
+
+namespace moe {
+namespace {
+
+constexpr int kRounds = 4;              // 32-element rounds per warp and chunk
+constexpr int kSmemBudget = 48 * 1024;  // per-warp counters of the scatter pass
+constexpr int kScanThreads = 1024;
+
+struct RouteShape {
+  int warps;      // warps per CTA of the hist / scatter passes
+  int64_t chunk;  // assignments per CTA
+  int64_t ctas;   // number of chunks
+};
+
+RouteShape route_shape(int64_t n, int32_t E) {
+  RouteShape s;
+  const int w = kSmemBudget / (4 * E);
+  s.warps = w > 16 ? 16 : (w < 1 ? 1 : w);
+  s.chunk = (int64_t)s.warps * kWarp * kRounds;
+  s.ctas = n > 0 ? (n + s.chunk - 1) / s.chunk : 1;
+  return s;
+}
+
+__device__ __forceinline__ int32_t load_expert(const int32_t* top_expert, int64_t p, int64_t n, int32_t E,
+                                               int32_t* status) {
+  if (p >= n) return -1;
+  const int32_t v = __ldg(top_expert + p);
+  if (v >= 0 && v < E) return v;
+  flag_status(status, MOE_STATUS_BAD_EXPERT);
+  return -1;
+}
+
+__global__ void route_hist_kernel(const int32_t* __restrict__ top_expert, int64_t n, int32_t E,
+                                  int32_t* __restrict__ counts, int32_t* status) {
+  extern __shared__ int32_t hist[];
+  for (int e = threadIdx.x; e < E; e += blockDim.x) hist[e] = 0;
+  __syncthreads();
+  const int warp = threadIdx.x / kWarp, lane = lane_id();
+  const int64_t base = (int64_t)blockIdx.x * blockDim.x * kRounds + (int64_t)warp * kWarp * kRounds;
+#pragma unroll
+  for (int r = 0; r < kRounds; ++r) {
+    const int32_t e = load_expert(top_expert, base + r * kWarp + lane, n, E, status);
+    const unsigned peers = __match_any_sync(0xffffffffu, e);
+    if (e >= 0 && lane == __ffs(peers) - 1) atomicAdd(&hist[e], __popc(peers));
+  }
+  __syncthreads();
+  for (int e = threadIdx.x; e < E; e += blockDim.x) counts[(int64_t)blockIdx.x * E + e] = hist[e];
+}
+
+// Single CTA. counts[g][e] becomes the first sorted position of chunk g's
+// assignments to expert e.
+__global__ void __launch_bounds__(kScanThreads) route_scan_kernel(int32_t* __restrict__ counts, int64_t G, int32_t E,
+                                                                   int32_t m, int32_t* __restrict__ bins,
+                                                                   int32_t* __restrict__ padded_bins) {
+  __shared__ int32_t start[MOE_MAX_EXPERTS];
+  __shared__ int64_t warp_sum[kScanThreads / kWarp][2];
+  // Column pass: exclusive prefix over chunks, total per expert.
+  for (int e = threadIdx.x; e < E; e += blockDim.x) {
+    int32_t run = 0;
+    int64_t g = 0;
+    for (; g + 8 <= G; g += 8) {
+      int32_t c[8];
+#pragma unroll
+      for (int q = 0; q < 8; ++q) c[q] = counts[(g + q) * E + e];
+#pragma unroll
+      for (int q = 0; q < 8; ++q) {
+        counts[(g + q) * E + e] = run;
+        run += c[q];
+      }
+    }
+    for (; g < G; ++g) {
+      const int32_t c = counts[g * E + e];
+      counts[g * E + e] = run;
+      run += c;
+    }
+    start[e] = run;  // total count of expert e for now
+  }
+  __syncthreads();
+  // Exclusive scan over experts of the counts and of the padded counts.
+  const int per = (E + kScanThreads - 1) / kScanThreads;
+  const int lo = threadIdx.x * per;
+  const int hi = min(lo + per, (int)E);
+  int64_t s = 0, ps = 0;
+  for (int e = lo; e < hi; ++e) {
+    const int64_t c = start[e];
+    s += c;
+    ps += (c + m - 1) / m * m;
+  }
+  const int lane = lane_id(), warp = threadIdx.x / kWarp;
+  int64_t xs = s, xps = ps;
+#pragma unroll
+  for (int d = 1; d < kWarp; d <<= 1) {
+    const int64_t a = __shfl_up_sync(0xffffffffu, xs, d);
+    const int64_t b = __shfl_up_sync(0xffffffffu, xps, d);
+    if (lane >= d) { xs += a; xps += b; }
+  }
+  if (lane == kWarp - 1) { warp_sum[warp][0] = xs; warp_sum[warp][1] = xps; }
+  __syncthreads();
+  if (warp == 0) {
+    int64_t a = warp_sum[lane][0], b = warp_sum[lane][1];
+#pragma unroll
+    for (int d = 1; d < kWarp; d <<= 1) {
+      const int64_t ua = __shfl_up_sync(0xffffffffu, a, d);
+      const int64_t ub = __shfl_up_sync(0xffffffffu, b, d);
+      if (lane >= d) { a += ua; b += ub; }
+    }
+    warp_sum[lane][0] = a;
+    warp_sum[lane][1] = b;
+  }
+  __syncthreads();
+  int64_t run = xs - s + (warp > 0 ? warp_sum[warp - 1][0] : 0);
+  int64_t prun = xps - ps + (warp > 0 ? warp_sum[warp - 1][1] : 0);
+  for (int e = lo; e < hi; ++e) {
+    const int64_t c = start[e];
+    start[e] = (int32_t)run;  // now the exclusive start of expert e
+    run += c;
+    prun += (c + m - 1) / m * m;
+    bins[e] = (int32_t)run;
+    if (padded_bins != nullptr) padded_bins[e] = (int32_t)prun;
+  }
+  __syncthreads();
+  for (int e = threadIdx.x; e < E; e += blockDim.x) {
+    const int32_t st = start[e];
+    for (int64_t g = 0; g < G; ++g) counts[g * E + e] += st;
+  }
+}
+
+__global__ void route_scatter_kernel(const int32_t* __restrict__ top_expert, int64_t n, int32_t E,
+                                     const int32_t* __restrict__ offsets, int32_t* __restrict__ indices,
+                                     int32_t* __restrict__ bin_ids, int32_t* __restrict__ positions) {
+  extern __shared__ int32_t whist[];  // [warps][E]: per-warp running offsets
+  const int warps = blockDim.x / kWarp;
+  const int warp = threadIdx.x / kWarp, lane = lane_id();
+  for (int q = threadIdx.x; q < warps * E; q += blockDim.x) whist[q] = 0;
+  __syncthreads();
+  const int64_t base = (int64_t)blockIdx.x * blockDim.x * kRounds + (int64_t)warp * kWarp * kRounds;
+  int32_t* mine = whist + warp * E;
+  int32_t ex[kRounds];
+#pragma unroll
+  for (int r = 0; r < kRounds; ++r) {
+    ex[r] = load_expert(top_expert, base + r * kWarp + lane, n, E, nullptr);
+    const unsigned peers = __match_any_sync(0xffffffffu, ex[r]);
+    if (ex[r] >= 0 && lane == __ffs(peers) - 1) mine[ex[r]] += __popc(peers);
+    __syncwarp();
+  }
+  __syncthreads();
+  for (int e = threadIdx.x; e < E; e += blockDim.x) {
+    int32_t run = offsets[(int64_t)blockIdx.x * E + e];
+    for (int w = 0; w < warps; ++w) {
+      const int32_t c = whist[w * E + e];
+      whist[w * E + e] = run;
+      run += c;
+    }
+  }
+  __syncthreads();
+  const unsigned lt = lanemask_lt();
+#pragma unroll
+  for (int r = 0; r < kRounds; ++r) {
+    const int32_t e = ex[r];
+    const unsigned peers = __match_any_sync(0xffffffffu, e);
+    if (e >= 0) {
+      const int32_t dst = mine[e] + __popc(peers & lt);
+      const int32_t a = (int32_t)(base + r * kWarp + lane);
+      indices[dst] = a;
+      bin_ids[dst] = e;
+      if (positions != nullptr) positions[a] = dst;
+    }
+    __syncwarp();
+    if (e >= 0 && lane == __ffs(peers) - 1) mine[e] += __popc(peers);
+    __syncwarp();
+  }
+}
+
+}  // namespace
+}  // namespace moe
+
+using namespace moe;
+
+extern "C" size_t moe_route_build_workspace_size(int64_t n, int32_t num_experts) {
+  if (n < 0 || num_experts < 1 || num_experts > MOE_MAX_EXPERTS) return 0;
+  const RouteShape s = route_shape(n, num_experts);
+  const size_t bytes = (size_t)s.ctas * (size_t)num_experts * sizeof(int32_t);
+  return (bytes + 255) / 256 * 256;
+}
+
+extern "C" int moe_route_build(const int32_t* top_expert, int64_t n, int32_t E, int32_t pad_multiple,
+                               int32_t* indices, int32_t* bin_ids, int32_t* bins, int32_t* padded_bins,
+                               int32_t* positions, void* workspace, size_t workspace_bytes, int32_t* d_status,
+                               moe_stream_t stream) {
+  if (n < 0 || n > INT32_MAX || E < 1 || E > MOE_MAX_EXPERTS || pad_multiple < 1) return MOE_ERR_INVALID_ARG;
+  if (n + (int64_t)E * (pad_multiple - 1) > INT32_MAX) return MOE_ERR_INVALID_ARG;
+  if (bins == nullptr || workspace == nullptr) return MOE_ERR_INVALID_ARG;
+  if (n > 0 && (top_expert == nullptr || indices == nullptr || bin_ids == nullptr)) return MOE_ERR_INVALID_ARG;
+  if (workspace_bytes < moe_route_build_workspace_size(n, E)) return MOE_ERR_INVALID_ARG;
+  const void* ptrs[] = {top_expert, indices, bin_ids, bins, padded_bins, positions, workspace, d_status};
+  for (const void* p : ptrs)
+    if (p != nullptr && !aligned(p, 4)) return MOE_ERR_UNSUPPORTED;
+
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  const RouteShape shape = route_shape(n, E);
+  int32_t* counts = static_cast<int32_t*>(workspace);
+  const int threads = shape.warps * kWarp;
+  route_hist_kernel<<<(unsigned)shape.ctas, threads, E * sizeof(int32_t), s>>>(top_expert, n, E, counts, d_status);
+  route_scan_kernel<<<1, kScanThreads, 0, s>>>(counts, shape.ctas, E, pad_multiple, bins, padded_bins);
+  if (n > 0)
+    route_scatter_kernel<<<(unsigned)shape.ctas, threads, (size_t)shape.warps * E * sizeof(int32_t), s>>>(
+        top_expert, n, E, counts, indices, bin_ids, positions);
+  return check_launch();
+}

@@ -1,0 +1,331 @@
+"""GPU parity: every entry point of the CUDA library against the CPU oracle,
+element by element, on the named workloads (tiny fp32, Mixtral-8x7B binned,
+Mixtral-8x22B padded, DeepSeek-V3 binned and padded, Qwen2-MoE-57B
+compaction) at full size and on an edge matrix (empty experts, capacity 0 /
+1 / max-1 / max, counts on and just over the padding multiple, TOP_K 1..40,
+hidden sizes with ragged tails, T = 0 and 1, misaligned pointers, poisoned
+padding rows, invalid device data reported through the status word).
+
+Gates: bit-exact for route build, gather, compaction and unweighted scatter;
+weighted scatter within 1e-5*(1+|ref|) for fp32 outputs and 2e-2 relative
+for bf16 outputs (and, by construction, bit-exact as well); wgrad within
+1e-5*(1+|ref|) (it is always an fp32 output).
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import padded_permute_combine_gb300 as p
+from padded_permute_combine_gb300 import _lib
+from padded_permute_combine_gb300 import workloads as wl
+from gpu_util import (assert_bits_equal, assert_close_bf16, assert_close_fp32, misaligned_like, to_dev,
+                      to_host)
+
+pytestmark = pytest.mark.gpu
+
+DEV = torch.device("cuda:0")
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib_loaded():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    p.load()
+    oracle.load()
+
+
+def status_word():
+    return torch.zeros(1, dtype=torch.int32, device=DEV)
+
+
+def check_scatter(got, want, what):
+    if got.dtype == np.float32:
+        assert_close_fp32(got, want, what)
+    else:
+        assert_close_bf16(got, want, what)
+    assert_bits_equal(got, want, what + " (bitwise)")
+
+
+def run_routing(r: wl.Routing, binned=True, padded=True, poison=True, misalign=False, pass_positions=True):
+    """Route build, then gather / scatter (weighted and not) / wgrad for both
+    layouts, each compared with the oracle on the same inputs."""
+    T, H, E, K = r.T, r.H, r.E, r.K
+    m = r.pad_multiple or 1
+    st = status_word()
+    te = to_dev(r.top_expert, DEV)
+    route = p.moe_route_build(te, E, m, status=st)
+    o = oracle.route_build(r.top_expert, E, m)
+    for k in ("indices", "bin_ids", "bins", "padded_bins", "positions"):
+        assert_bits_equal(to_host(getattr(route, k)), o[k], "%s route.%s" % (r.name, k))
+    x = to_dev(r.x, DEV)
+    grad = to_dev(r.grad, DEV)
+    if misalign:
+        x, grad = misaligned_like(x), misaligned_like(grad)
+    w = to_dev(r.weights.reshape(-1), DEV)
+    pos = route.positions if pass_positions else None
+
+    if binned:
+        cap = r.capacity
+        xb = p.moe_binned_gather(x, route.indices, route.bins, E, cap, K, status=st)
+        o_xb = oracle.binned_gather(r.x, o["indices"], o["bin_ids"], o["bins"], E, cap, K)
+        assert_bits_equal(to_host(xb), o_xb, r.name + " binned_gather")
+        xe_np = wl.expert_rows(E * cap, H, r.dtype, r.seed).reshape(E, cap, H)
+        if poison and cap > 0:
+            # unused capacity rows hold NaN: scatter and wgrad must never read them
+            kept = np.zeros(E * cap, bool)
+            counts = np.diff(np.concatenate([[0], o["bins"]]))
+            for e in range(E):
+                kept[e * cap: e * cap + min(counts[e], cap)] = True
+            flat = xe_np.reshape(E * cap, H)
+            flat[~kept] = np.float32(np.nan) if r.dtype == wl.F32 else np.uint16(0x7FC0)
+        xe = to_dev(xe_np, DEV)
+        if misalign:
+            xe = misaligned_like(xe)
+        for weights, o_w, tag in ((w, r.weights, "weighted"), (None, None, "unweighted")):
+            y = p.moe_binned_scatter(xe, route.indices, route.bin_ids, route.bins, weights, T, K, positions=pos,
+                                     status=st)
+            o_y = oracle.binned_scatter(xe_np, o["indices"], o["bin_ids"], o["bins"], o_w, T, K)
+            assert not np.isnan(oracle.to_f32(o_y)).any()
+            check_scatter(to_host(y), o_y, "%s binned_scatter %s" % (r.name, tag))
+        wg = p.moe_binned_wgrad(xe, grad, route.indices, route.bin_ids, route.bins, K, status=st)
+        o_wg = oracle.binned_wgrad(xe_np, r.grad, o["indices"], o["bin_ids"], o["bins"], K)
+        assert_close_fp32(to_host(wg), o_wg, r.name + " binned_wgrad")
+
+    if padded:
+        P = int(o["padded_bins"][-1]) if E else 0
+        xp = p.moe_padded_gather(x, route.indices, route.bins, route.padded_bins, K, out_rows=P, status=st)
+        o_xp = oracle.padded_gather(r.x, o["indices"], o["bin_ids"], o["bins"], o["padded_bins"], K)
+        assert_bits_equal(to_host(xp), o_xp, r.name + " padded_gather")
+        xe_np = wl.expert_rows(P, H, r.dtype, r.seed)
+        if poison:
+            real = np.zeros(P, bool)
+            starts = np.concatenate([[0], o["padded_bins"][:-1]])
+            counts = np.diff(np.concatenate([[0], o["bins"]]))
+            for e in range(E):
+                real[starts[e]: starts[e] + counts[e]] = True
+            xe_np[~real] = np.float32(np.nan) if r.dtype == wl.F32 else np.uint16(0x7FC0)
+        xe = to_dev(xe_np, DEV)
+        if misalign:
+            xe = misaligned_like(xe)
+        for weights, o_w, tag in ((w, r.weights, "weighted"), (None, None, "unweighted")):
+            y = p.moe_padded_scatter(xe, route.indices, route.bin_ids, route.bins, route.padded_bins, weights, T, K,
+                                     positions=pos, status=st)
+            o_y = oracle.padded_scatter(xe_np, o["indices"], o["bin_ids"], o["bins"], o["padded_bins"], o_w, T, K)
+            check_scatter(to_host(y), o_y, "%s padded_scatter %s" % (r.name, tag))
+        wg = p.moe_padded_wgrad(xe, grad, route.indices, route.bin_ids, route.bins, route.padded_bins, K, status=st)
+        o_wg = oracle.padded_wgrad(xe_np, r.grad, o["indices"], o["bin_ids"], o["bins"], o["padded_bins"], K)
+        assert_close_fp32(to_host(wg), o_wg, r.name + " padded_wgrad")
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0, "device status %d on valid input" % int(st.item())
+
+
+# ------------------------------------------------------------ named workloads
+
+def test_pr1_tiny_f32():
+    run_routing(wl.pr1())
+
+
+def test_pr1_tiny_f32_without_positions():
+    run_routing(wl.pr1(seed=3), pass_positions=False)
+
+
+@pytest.mark.slow
+def test_mixtral_8x7b_binned_bf16():
+    run_routing(wl.mixtral_8x7b(), padded=True)
+
+
+@pytest.mark.slow
+def test_mixtral_8x22b_padded_bf16():
+    r = wl.mixtral_8x22b_padded()
+    counts = np.bincount(r.top_expert.reshape(-1), minlength=r.E)
+    assert sorted(counts.tolist())[:3] == [0, 1024, 1025]
+    run_routing(r, binned=False)
+
+
+@pytest.mark.slow
+def test_deepseek_v3_bf16():
+    r = wl.deepseek_v3()
+    run_routing(r, pass_positions=False)
+
+
+@pytest.mark.slow
+def test_deepseek_v3_with_empty_experts_bf16():
+    r = wl.deepseek_v3(seed=1, n_empty=32)
+    assert (np.bincount(r.top_expert.reshape(-1), minlength=r.E) == 0).sum() >= 32
+    run_routing(r)
+
+
+# ------------------------------------------------------------ edge matrix
+
+@pytest.mark.parametrize("H", [1, 7, 8, 255, 1003, 7168])
+@pytest.mark.parametrize("dtype", [wl.F32, wl.BF16])
+def test_hidden_sizes(H, dtype):
+    r = wl.uniform_routing("h%d" % H, 37, H, 6, 2, dtype, capacity=9, pad_multiple=4, seed=H)
+    run_routing(r)
+
+
+@pytest.mark.parametrize("K", [1, 2, 4, 8, 33, 40])
+def test_top_k_values(K):
+    r = wl.uniform_routing("k%d" % K, 29, 24, 48, K, wl.BF16, capacity=5, pad_multiple=8, seed=K)
+    run_routing(r)
+
+
+def test_capacity_edges():
+    base = wl.zipf_routing("cap", 300, 40, 16, 4, wl.F32, pad_multiple=3, seed=5)
+    maxc = int(np.bincount(base.top_expert.reshape(-1), minlength=16).max())
+    for cap in (0, 1, maxc - 1, maxc, maxc + 5):
+        base.capacity = cap
+        run_routing(base, padded=(cap == 0))
+
+
+def test_empty_experts_and_single_expert():
+    r = wl.uniform_routing("even", 64, 16, 8, 2, wl.BF16, capacity=12, pad_multiple=8, distinct=False, seed=2)
+    r.top_expert = (r.top_expert // 2 * 2).astype(np.int32)  # odd experts empty
+    run_routing(r)
+    r1 = wl.uniform_routing("one", 50, 16, 1, 1, wl.F32, capacity=20, pad_multiple=16, seed=4)
+    run_routing(r1)
+
+
+def test_counts_on_and_over_the_padding_multiple():
+    r = wl.padded_edge_routing("pad-edge", 300, 24, 7, 2, wl.BF16, pad_multiple=16, j=4, seed=6)
+    counts = np.bincount(r.top_expert.reshape(-1), minlength=7)
+    assert 0 in counts and 64 in counts and 65 in counts
+    run_routing(r, binned=False)
+
+
+def test_one_token_and_ragged_chunks():
+    run_routing(wl.uniform_routing("t1", 1, 40, 4, 2, wl.F32, capacity=1, pad_multiple=2, seed=7))
+    # n not a multiple of any block size; many route-build chunks
+    run_routing(wl.zipf_routing("ragged", 2053, 16, 64, 3, wl.BF16, capacity=50, pad_multiple=32, seed=8))
+
+
+def test_no_tokens():
+    E = 5
+    te = torch.zeros(0, dtype=torch.int32, device=DEV)
+    route = p.moe_route_build(te, E, 4)
+    assert to_host(route.bins).tolist() == [0] * E and to_host(route.padded_bins).tolist() == [0] * E
+    x = torch.zeros((0, 8), dtype=torch.float32, device=DEV)
+    xb = p.moe_binned_gather(x, route.indices, route.bins, E, 3, 2)
+    assert to_host(xb).shape == (E, 3, 8) and not to_host(xb).any()
+
+
+def test_misaligned_pointers_take_narrow_vectors():
+    run_routing(wl.uniform_routing("mis-bf16", 40, 64, 6, 2, wl.BF16, capacity=10, pad_multiple=4, seed=9),
+                misalign=True)
+    run_routing(wl.uniform_routing("mis-f32", 40, 64, 6, 2, wl.F32, capacity=10, pad_multiple=4, seed=10),
+                misalign=True)
+
+
+def test_large_route_build_many_chunks():
+    g = np.random.default_rng(11)
+    for n, E in [(200_003, 256), (70_001, 4096), (65_536, 1), (131_072, 3000)]:
+        te = g.integers(0, E, size=n).astype(np.int32)
+        route = p.moe_route_build(to_dev(te, DEV), E, 128)
+        o = oracle.route_build(te, E, 128)
+        for k in ("indices", "bin_ids", "bins", "padded_bins", "positions"):
+            assert_bits_equal(to_host(getattr(route, k)), o[k], "n=%d E=%d %s" % (n, E, k))
+
+
+# ------------------------------------------------------------ compaction
+
+def run_compaction(d: wl.DenseRoutes, status_expected=0):
+    probs = to_dev(d.probs, DEV)
+    rmap = to_dev(d.routing_map, DEV)
+    pi, idx = p.moe_routing_map_to_indices_fwd(probs, rmap, d.topk)
+    o_pi, o_idx = oracle.routing_map_to_indices_fwd(d.probs, d.routing_map, d.topk)
+    assert_bits_equal(to_host(idx), o_idx, d.name + " indices")
+    assert_bits_equal(to_host(pi), o_pi, d.name + " probs_indices")
+    st = status_word()
+    gp = p.moe_routing_map_to_indices_bwd(to_dev(d.grad_probs_indices, DEV), idx, d.E, status=st)
+    o_gp = oracle.routing_map_to_indices_bwd(d.grad_probs_indices, o_idx, d.E)
+    assert_bits_equal(to_host(gp), o_gp, d.name + " grad_probs")
+    assert int(st.item()) == status_expected
+
+
+@pytest.mark.slow
+def test_qwen2_moe_57b_compaction():
+    run_compaction(wl.qwen2_moe_57b())
+
+
+@pytest.mark.parametrize("T,E,topk,max_routes", [(1, 1, 1, 1), (333, 5, 3, 5), (1000, 64, 8, 12), (257, 160, 6, 6),
+                                                 (100, 37, 40, 37), (513, 256, 8, 8)])
+def test_compaction_shapes(T, E, topk, max_routes):
+    run_compaction(wl.dense_routes("c", T, E, topk, max_routes=max_routes, seed=T + E))
+
+
+def test_compaction_from_routing_and_misaligned_map():
+    d = wl.dense_from_routing(wl.deepseek_v3(seed=2))
+    run_compaction(d)
+    probs = to_dev(d.probs, DEV)
+    rmap = misaligned_like(to_dev(d.routing_map, DEV), 3)
+    pi, idx = p.moe_routing_map_to_indices_fwd(probs, rmap, d.topk)
+    o_pi, o_idx = oracle.routing_map_to_indices_fwd(d.probs, d.routing_map, d.topk)
+    assert_bits_equal(to_host(idx), o_idx, "misaligned map indices")
+    assert_bits_equal(to_host(pi), o_pi, "misaligned map probs")
+
+
+def test_compaction_bool_map():
+    d = wl.dense_routes("bool", 200, 32, 4, max_routes=6, seed=1)
+    probs = to_dev(d.probs, DEV)
+    rmap = to_dev(d.routing_map.astype(bool), DEV)
+    pi, idx = p.moe_routing_map_to_indices_fwd(probs, rmap, d.topk)
+    o_pi, o_idx = oracle.routing_map_to_indices_fwd(d.probs, d.routing_map, d.topk)
+    assert_bits_equal(to_host(idx), o_idx, "bool map")
+
+
+# ------------------------------------------------------------ invalid device data
+
+def test_bad_expert_ids_are_reported_not_faulted():
+    te = np.array([0, 1, 5, -1, 2, 3, 1, 0], np.int32)
+    st = status_word()
+    p.moe_route_build(to_dev(te, DEV), 4, 2, status=st)
+    torch.cuda.synchronize()
+    assert int(st.item()) & _lib.MOE_STATUS_BAD_EXPERT
+
+
+def test_corrupt_bins_and_positions_are_reported():
+    r = wl.uniform_routing("corrupt", 32, 16, 4, 2, wl.F32, capacity=8, pad_multiple=4, seed=12)
+    route = p.moe_route_build(to_dev(r.top_expert, DEV), 4, 4)
+    x = to_dev(r.x, DEV)
+    bad_bins = torch.tensor([40, 10, 70, 64], dtype=torch.int32, device=DEV)
+    st = status_word()
+    p.moe_binned_gather(x, route.indices, bad_bins, 4, 8, 2, status=st)
+    p.moe_padded_gather(x, route.indices, bad_bins, torch.tensor([4, 8, 12, 16], dtype=torch.int32, device=DEV),
+                        2, out_rows=16, status=st)
+    torch.cuda.synchronize()
+    assert int(st.item()) & _lib.MOE_STATUS_BAD_BINS
+    st.zero_()
+    bad_pos = torch.full((64,), 1 << 20, dtype=torch.int32, device=DEV)
+    xe = torch.randn(4, 8, 16, device=DEV)
+    y = p.moe_binned_scatter(xe, route.indices, route.bin_ids, route.bins, None, 32, 2, positions=bad_pos, status=st)
+    torch.cuda.synchronize()
+    assert int(st.item()) & _lib.MOE_STATUS_BAD_INDEX
+    assert not to_host(y).any()  # every slot skipped
+    st.zero_()
+    pb = torch.tensor([4, 8, 12, 20], dtype=torch.int32, device=DEV)
+    p.moe_padded_gather(x, route.indices, route.bins, pb, 2, out_rows=12, status=st)
+    torch.cuda.synchronize()
+    assert int(st.item()) & _lib.MOE_STATUS_ROWS_MISMATCH
+
+
+def test_compaction_bwd_bad_index_reported():
+    idx = torch.tensor([[0, 7], [1, -1]], dtype=torch.int32, device=DEV)
+    g = torch.tensor([[1.0, 2.0], [3.0, 4.0]], device=DEV)
+    st = status_word()
+    gp = p.moe_routing_map_to_indices_bwd(g, idx, 4, status=st)
+    torch.cuda.synchronize()
+    assert int(st.item()) & _lib.MOE_STATUS_BAD_INDEX
+    assert to_host(gp).tolist() == [[1.0, 0, 0, 0], [0, 3.0, 0, 0]]
+
+
+def test_error_codes_through_the_binding():
+    x = torch.zeros((4, 8), dtype=torch.float16, device=DEV)
+    with pytest.raises(TypeError):
+        p.moe_binned_gather(x, torch.zeros(8, dtype=torch.int32, device=DEV),
+                            torch.zeros(2, dtype=torch.int32, device=DEV), 2, 2, 2)
+    xs = torch.zeros((4, 8), device=DEV)
+    with pytest.raises(p.MoeError) as ei:
+        p.moe_binned_gather(xs, torch.zeros(8, dtype=torch.int32, device=DEV),
+                            torch.zeros(2, dtype=torch.int32, device=DEV), 2, -1, 2)
+    assert ei.value.code == _lib.MOE_ERR_INVALID_ARG

@@ -1,0 +1,532 @@
+"""Benchmark of the MoE routing path on GB300.
+
+One step = one pass of the whole routing path over one DeepSeek-V3-shaped
+batch (T=8192 tokens, H=7168, E=256 experts, TOP_K=8, capacity 256, padding
+multiple 128, bf16 activations, Zipf(1.1) expert popularity):
+  routing-map compaction -> route build -> binned gather -> binned scatter
+  (weighted) -> binned wgrad -> padded gather -> padded scatter (weighted)
+  -> padded wgrad -> compaction backward.
+The expert FFN between gather and scatter is the identity (it is not part of
+the routing path), so scatter combines the gathered rows themselves.
+
+Prints one JSON line. ``value`` = routed assignments (rows) per second over
+the whole step, inputs resident in HBM, L2 flushed (512 MB write) before
+every step. ``e2e`` = the same metric through the public API with pinned
+host buffers: host->device copies of the inputs and device->host copies of
+the combined outputs and the dense router gradient inside the timed region.
+``roofline`` reports the dominant kernel against the measured HBM copy
+bandwidth. ``cpu_baseline`` times the CPU oracle on a token subset of the
+same workload on one host core.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from padded_permute_combine_gb300 import workloads as wl  # noqa: E402
+
+METRIC = "routed rows/sec and achieved HBM GB/s (% of GB300 peak), gather+scatter+wgrad"
+UNIT = "rows/s"
+L2_FLUSH_BYTES = 512 << 20
+FALLBACK_HBM_GBS = 6800.0
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--e2e-steps", type=int, default=20)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--profile-case", action="store_true",
+                    help="no timing: run each op of a smaller batch twice, for an ncu capture")
+    ap.add_argument("--tokens", type=int, default=4096, help="tokens of the --profile-case batch")
+    a = ap.parse_args()
+    a.warmup = max(3, a.warmup)
+    a.steps = max(1, a.steps)
+    return a
+
+
+def workload(seed: int, tokens: int | None = None):
+    r = wl.deepseek_v3(seed=seed)
+    if tokens is not None and tokens < r.T:
+        # the first `tokens` tokens of the same batch, capacity ceil(T*K/E)
+        r = wl.Routing(r.name + "-t%d" % tokens, tokens, r.H, r.E, r.K, r.dtype, math.ceil(tokens * r.K / r.E),
+                       r.pad_multiple, r.top_expert[:tokens].copy(), r.weights[:tokens].copy(), r.seed)
+    return r, wl.dense_from_routing(r)
+
+
+def workload_config(r) -> dict:
+    return {"workload": "deepseek-v3-shaped MoE routing, T=%d H=%d E=%d top_k=%d capacity=%d pad_multiple=%d "
+                        "bf16, Zipf(1.1) popularity" % (r.T, r.H, r.E, r.K, r.capacity, r.pad_multiple),
+            "tokens": r.T, "hidden": r.H, "experts": r.E, "top_k": r.K, "capacity": r.capacity,
+            "pad_multiple": r.pad_multiple,
+            "l2": "flushed before every step (512 MB write); inputs > L2 in total",
+            "expert_ffn": "identity (not part of the routing path)"}
+
+
+def measured_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def traffic_from_profiles(kernel: str, digest: str):
+    """dram read+write bytes per launch of `kernel`, from the committed ncu
+    summary, if it was taken on the current sources."""
+    path = os.path.join(ROOT, "profiles", "dram_traffic.txt")
+    try:
+        for line in open(path):
+            f = line.split()
+            if len(f) >= 3 and f[0] == kernel and f[1] == digest:
+                return int(float(f[2]))
+    except OSError:
+        pass
+    return None
+
+
+# ------------------------------------------------------------------ GPU arm
+
+class Path:
+    """Device buffers and the launches of one step."""
+
+    def __init__(self, r, d, dev):
+        import torch
+
+        import padded_permute_combine_gb300 as p
+        from padded_permute_combine_gb300 import ops
+
+        self.p, self.torch = p, torch
+        self.r, self.d, self.dev = r, d, dev
+        T, H, E, K = r.T, r.H, r.E, r.K
+        self.n = T * K
+        bf = torch.bfloat16
+
+        def dev_bf16(a):
+            return torch.from_numpy(a.view(np.int16)).to(dev).view(bf)
+
+        self.probs = torch.from_numpy(d.probs).to(dev)
+        self.rmap = torch.from_numpy(d.routing_map).to(dev)
+        self.x = dev_bf16(r.x)
+        self.grad = dev_bf16(r.grad)
+        self.pi = torch.empty((T, K), dtype=torch.float32, device=dev)
+        self.idx = torch.empty((T, K), dtype=torch.int32, device=dev)
+        n = self.n
+        self.route = p.Route(torch.empty(n, dtype=torch.int32, device=dev),
+                             torch.empty(n, dtype=torch.int32, device=dev),
+                             torch.empty(E, dtype=torch.int32, device=dev),
+                             torch.empty(E, dtype=torch.int32, device=dev),
+                             torch.empty(n, dtype=torch.int32, device=dev))
+        self.ws = ops.route_workspace(n, E, dev)
+        self.xb = torch.empty((E, r.capacity, H), dtype=bf, device=dev)
+        self.yb = torch.empty((T, H), dtype=bf, device=dev)
+        self.yp = torch.empty((T, H), dtype=bf, device=dev)
+        self.wgb = torch.empty(n, dtype=torch.float32, device=dev)
+        self.wgp = torch.empty(n, dtype=torch.float32, device=dev)
+        self.gprobs = torch.empty((T, E), dtype=torch.float32, device=dev)
+        # The padded row count is data dependent: size the buffer from one
+        # route build of this (fixed) batch.
+        self.front()
+        torch.cuda.synchronize(dev)
+        self.P = int(self.route.padded_bins[-1].item())
+        self.xp = torch.empty((self.P, H), dtype=bf, device=dev)
+        counts = np.diff(np.concatenate([[0], self.route.bins.cpu().numpy()]))
+        self.kept = int(np.minimum(counts, r.capacity).sum())
+
+    def front(self):
+        p, r = self.p, self.r
+        p.moe_routing_map_to_indices_fwd(self.probs, self.rmap, r.K, out=(self.pi, self.idx))
+        p.moe_route_build(self.idx, r.E, r.pad_multiple, workspace=self.ws, out=self.route)
+
+    def ops(self):
+        """(name, launches, callable) for the step, in order."""
+        p, r, rt = self.p, self.r, self.route
+        T, E, K = r.T, r.E, r.K
+        w = self.pi.view(-1)
+        return [
+            ("compaction_fwd", 1, lambda: p.moe_routing_map_to_indices_fwd(self.probs, self.rmap, K,
+                                                                           out=(self.pi, self.idx))),
+            ("route_build", 3, lambda: p.moe_route_build(self.idx, E, r.pad_multiple, workspace=self.ws, out=rt)),
+            ("binned_gather", 1, lambda: p.moe_binned_gather(self.x, rt.indices, rt.bins, E, r.capacity, K,
+                                                             out=self.xb)),
+            ("binned_scatter", 1, lambda: p.moe_binned_scatter(self.xb, rt.indices, rt.bin_ids, rt.bins, w, T, K,
+                                                               positions=rt.positions, out=self.yb)),
+            ("binned_wgrad", 1, lambda: p.moe_binned_wgrad(self.xb, self.grad, rt.indices, rt.bin_ids, rt.bins, K,
+                                                           out=self.wgb)),
+            ("padded_gather", 1, lambda: p.moe_padded_gather(self.x, rt.indices, rt.bins, rt.padded_bins, K,
+                                                             out_rows=self.P, out=self.xp)),
+            ("padded_scatter", 1, lambda: p.moe_padded_scatter(self.xp, rt.indices, rt.bin_ids, rt.bins,
+                                                               rt.padded_bins, w, T, K, positions=rt.positions,
+                                                               out=self.yp)),
+            ("padded_wgrad", 1, lambda: p.moe_padded_wgrad(self.xp, self.grad, rt.indices, rt.bin_ids, rt.bins,
+                                                           rt.padded_bins, K, out=self.wgp)),
+            ("compaction_bwd", 1, lambda: p.moe_routing_map_to_indices_bwd(self.wgp.view(T, K), self.idx, E,
+                                                                           out=self.gprobs)),
+        ]
+
+    def algorithmic_bytes(self) -> dict:
+        """Bytes each kernel must move (no reuse credited), per launch."""
+        r = self.r
+        T, H, E, K, n, b = r.T, r.H, r.E, r.K, self.n, 2
+        kept, P, cap = self.kept, self.P, r.capacity
+        return {
+            "compaction_fwd": T * E + T * K * 4 + T * K * 8,
+            "route_build": 2 * 4 * n + 12 * n + 8 * E,
+            "binned_gather": kept * H * b + E * cap * H * b + 4 * kept + 4 * E,
+            "binned_scatter": kept * H * b + T * H * b + 12 * n + 4 * E,
+            "binned_wgrad": 2 * kept * H * b + 12 * n + 4 * E,
+            "padded_gather": n * H * b + P * H * b + 4 * n + 8 * E,
+            "padded_scatter": n * H * b + T * H * b + 12 * n + 8 * E,
+            "padded_wgrad": 2 * n * H * b + 12 * n + 8 * E,
+            "compaction_bwd": T * K * 8 + T * E * 4,
+        }
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons while the timed region runs."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index), "--query-gpu=" + self.FIELDS,
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *exc):
+        self.lines = []
+        if self.proc is not None:
+            time.sleep(0.15)
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                out, _ = self.proc.communicate()
+            self.lines = [ln for ln in out.splitlines() if ln.strip()]
+
+    def summary(self):
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        sm, mx, reasons = [], [], set()
+        for ln in self.lines:
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 7:
+                continue
+            try:
+                sm.append(float(f[0]))
+                mx.append(float(f[1]))
+            except ValueError:
+                continue
+            for nm, v in zip(names, f[3:7]):
+                if v.lower().startswith("active"):
+                    reasons.add(nm)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def run_gpu(args, rank, world, local_rank):
+    import torch
+
+    import padded_permute_combine_gb300 as p
+
+    p.load()  # fails loudly when the CUDA library is missing
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.init_process_group("nccl", device_id=dev)
+    r, d = workload(seed=rank)
+    path = Path(r, d, dev)
+    ops = path.ops()
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.int32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def barrier():
+        torch.cuda.synchronize(dev)
+        if dist is not None:
+            dist.barrier()
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        for _, _, f in ops:
+            f()
+    barrier()
+
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(len(ops) + 1)] for _ in range(args.steps)]
+    with ClockSampler(local_rank) as clocks:
+        barrier()
+        t_host = time.perf_counter()
+        for s in range(args.steps):
+            flush.zero_()
+            ev[s][0].record(stream)
+            for q, (_, _, f) in enumerate(ops):
+                f()
+                ev[s][q + 1].record(stream)
+        barrier()
+        t_host = time.perf_counter() - t_host
+    per_kernel = {name: [] for name, _, _ in ops}
+    step_ms = []
+    for s in range(args.steps):
+        step_ms.append(ev[s][0].elapsed_time(ev[s][-1]))
+        for q, (name, _, _) in enumerate(ops):
+            per_kernel[name].append(ev[s][q].elapsed_time(ev[s][q + 1]))
+    total_ms = float(sum(step_ms))
+    if dist is not None:
+        t = torch.tensor([total_ms], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+
+    e2e = run_e2e(args, path, dev, dist)
+
+    if rank != 0:
+        if dist is not None:
+            dist.barrier()
+            dist.destroy_process_group()
+        return
+    n = path.n
+    ms_per_step = total_ms / args.steps
+    value = world * n * args.steps / (total_ms / 1e3)
+    peak, peak_kind = measured_peak()
+    algo = path.algorithmic_bytes()
+    kern = {}
+    for name, launches, _ in ops:
+        ms = statistics.mean(per_kernel[name])
+        gbs = algo[name] / (ms * 1e-3) / 1e9
+        kern[name] = {"ms": round(ms, 5), "algorithmic_bytes": algo[name], "gbs": round(gbs, 1),
+                      "frac_of_%s_peak" % peak_kind: round(gbs / peak, 4), "launches": launches}
+    hot = ["binned_gather", "binned_scatter", "binned_wgrad", "padded_gather", "padded_scatter", "padded_wgrad"]
+    hot_bytes = sum(algo[k] for k in hot)
+    hot_ms = sum(kern[k]["ms"] for k in hot)
+    dominant = max(kern, key=lambda k: kern[k]["ms"])
+    from padded_permute_combine_gb300 import build as libbuild
+
+    ach = kern[dominant]["gbs"]
+    line = {
+        "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": workload_config(r),
+        "hbm_gbs_gather_scatter_wgrad": round(hot_bytes / (hot_ms * 1e-3) / 1e9, 1),
+        "kernels": kern,
+        "roofline": {"bound": "hbm", "kernel": dominant, "achieved": ach, "peak": peak, "peak_kind": peak_kind,
+                     "unit": "GB/s", "frac": round(ach / peak, 4),
+                     "traffic": traffic_from_profiles(dominant, libbuild.source_digest())},
+        "e2e": e2e,
+        "gpu_launches": sum(l for _, l, _ in ops) * args.steps,
+        "clocks": clocks.summary(),
+        "host_timed_s": round(t_host, 4),
+        "kept_rows_binned": path.kept, "padded_rows": path.P, "assignments_per_step": n,
+    }
+    if not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(budget_s=12.0)
+    print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+def run_e2e(args, path, dev, dist):
+    """The same step through the public API from pinned host buffers:
+    inputs copied host->device, padded row count read back, outputs copied
+    device->host, all inside the timed region."""
+    import torch
+
+    p, r = path.p, path.r
+    T, E, K = r.T, r.E, r.K
+    stream = torch.cuda.current_stream(dev)
+    h_in = {"probs": path.probs.cpu().pin_memory(), "rmap": path.rmap.cpu().pin_memory(),
+            "x": path.x.cpu().pin_memory(), "grad": path.grad.cpu().pin_memory()}
+    h_out = {"yb": torch.empty_like(path.yb, device="cpu").pin_memory(),
+             "yp": torch.empty_like(path.yp, device="cpu").pin_memory(),
+             "gprobs": torch.empty_like(path.gprobs, device="cpu").pin_memory()}
+    h_p = torch.empty(1, dtype=torch.int32).pin_memory()
+    d_in = {k: torch.empty_like(v, device=dev) for k, v in h_in.items()}
+
+    def step():
+        for k in h_in:
+            d_in[k].copy_(h_in[k], non_blocking=True)
+        pi, idx = p.moe_routing_map_to_indices_fwd(d_in["probs"], d_in["rmap"], K)
+        rt = p.moe_route_build(idx, E, r.pad_multiple, workspace=path.ws)
+        h_p.copy_(rt.padded_bins[-1:], non_blocking=True)
+        stream.synchronize()
+        P = int(h_p.item())
+        w = pi.view(-1)
+        xb = p.moe_binned_gather(d_in["x"], rt.indices, rt.bins, E, r.capacity, K)
+        yb = p.moe_binned_scatter(xb, rt.indices, rt.bin_ids, rt.bins, w, T, K, positions=rt.positions)
+        p.moe_binned_wgrad(xb, d_in["grad"], rt.indices, rt.bin_ids, rt.bins, K)
+        xp = p.moe_padded_gather(d_in["x"], rt.indices, rt.bins, rt.padded_bins, K, out_rows=P)
+        yp = p.moe_padded_scatter(xp, rt.indices, rt.bin_ids, rt.bins, rt.padded_bins, w, T, K,
+                                  positions=rt.positions)
+        wgp = p.moe_padded_wgrad(xp, d_in["grad"], rt.indices, rt.bin_ids, rt.bins, rt.padded_bins, K)
+        gp = p.moe_routing_map_to_indices_bwd(wgp.view(T, K), idx, E)
+        h_out["yb"].copy_(yb, non_blocking=True)
+        h_out["yp"].copy_(yp, non_blocking=True)
+        h_out["gprobs"].copy_(gp, non_blocking=True)
+
+    for _ in range(3):
+        step()
+    torch.cuda.synchronize(dev)
+    if dist is not None:
+        dist.barrier()
+    steps = max(1, min(args.e2e_steps, args.steps))
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for _ in range(steps):
+        step()
+    t1.record(stream)
+    torch.cuda.synchronize(dev)
+    ms = t0.elapsed_time(t1)
+    if dist is not None:
+        t = torch.tensor([ms], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    world = dist.get_world_size() if dist is not None else 1
+    h2d = sum(v.numel() * v.element_size() for v in h_in.values())
+    d2h = sum(v.numel() * v.element_size() for v in h_out.values()) + 4
+    return {"value": round(world * path.n * steps / (ms * 1e-3), 1), "unit": UNIT, "steps": steps,
+            "ms_per_step": round(ms / steps, 5), "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+
+
+# ------------------------------------------------------------------ CPU oracle
+
+def oracle_step(r, d, T_s):
+    """The routing path on the oracle for the first T_s tokens of the batch."""
+    import oracle
+
+    K, E, H = r.K, r.E, r.H
+    cap = math.ceil(T_s * K / E)
+    probs, rmap = d.probs[:T_s], d.routing_map[:T_s]
+    x, grad = r.x[:T_s], r.grad[:T_s]
+    pi, idx = oracle.routing_map_to_indices_fwd(probs, rmap, K)
+    o = oracle.route_build(idx, E, r.pad_multiple)
+    w = pi.reshape(-1)
+    xb = oracle.binned_gather(x, o["indices"], o["bin_ids"], o["bins"], E, cap, K)
+    oracle.binned_scatter(xb, o["indices"], o["bin_ids"], o["bins"], w, T_s, K)
+    oracle.binned_wgrad(xb, grad, o["indices"], o["bin_ids"], o["bins"], K)
+    xp = oracle.padded_gather(x, o["indices"], o["bin_ids"], o["bins"], o["padded_bins"], K)
+    oracle.padded_scatter(xp, o["indices"], o["bin_ids"], o["bins"], o["padded_bins"], w, T_s, K)
+    wgp = oracle.padded_wgrad(xp, grad, o["indices"], o["bin_ids"], o["bins"], o["padded_bins"], K)
+    oracle.routing_map_to_indices_bwd(wgp.reshape(T_s, K), idx, E)
+    return T_s * K
+
+
+def _sample_tokens(r, d, budget_s):
+    """Tokens per oracle step so that one step takes about budget_s."""
+    oracle_step(r, d, 256)  # first touch of the inputs and the oracle's buffers
+    t0 = time.perf_counter()
+    oracle_step(r, d, 256)
+    dt = max(time.perf_counter() - t0, 1e-3)
+    return int(max(64, min(r.T, 256 * budget_s / dt)))
+
+
+def cpu_baseline(budget_s: float):
+    import oracle
+
+    oracle.build()
+    r, d = workload(seed=0)
+    T_s = _sample_tokens(r, d, budget_s / 2)
+    t0 = time.perf_counter()
+    rows = oracle_step(r, d, T_s)
+    rows += oracle_step(r, d, T_s)
+    dt = time.perf_counter() - t0
+    return {"value": round(rows / dt, 1), "unit": UNIT, "cores": 1, "kind": "oracle",
+            "sample": "first %d of %d tokens of the same batch (capacity ceil(T*K/E)), full path, 2 passes, "
+                      "single-threaded C oracle, %.1f s" % (T_s, r.T, dt)}
+
+
+def run_reference(args, rank):
+    """The oracle as the reference arm: rank 0 only, host cores."""
+    if rank != 0:
+        return
+    import oracle
+
+    oracle.build()
+    r, d = workload(seed=0)
+    per_step = max(0.5, min(10.0, 150.0 / (args.steps + args.warmup)))
+    T_s = _sample_tokens(r, d, per_step)
+    for _ in range(args.warmup):
+        oracle_step(r, d, T_s)
+    t0 = time.perf_counter()
+    rows = 0
+    for _ in range(args.steps):
+        rows += oracle_step(r, d, T_s)
+    dt = time.perf_counter() - t0
+    value = rows / dt
+    sample = "first %d of %d tokens of the same batch per step, full routing path, single-threaded C oracle" % (
+        T_s, r.T)
+    line = {"impl": "reference", "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(dt / args.steps * 1e3, 3),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": workload_config(r),
+            "cpu_baseline": {"value": round(value, 1), "unit": UNIT, "cores": 1, "kind": "oracle", "sample": sample},
+            "e2e": {"value": round(value, 1), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def run_profile_case(args):
+    """Each op of a `--tokens`-token batch once as warm-up, then the padded
+    gather, scatter and wgrad once more: three launches for `ncu -s 3 -c 3`
+    on the gather/scatter/wgrad kernels."""
+    import torch
+
+    dev = torch.device("cuda", 0)
+    r, d = workload(seed=0, tokens=args.tokens)
+    path = Path(r, d, dev)
+    ops = dict((name, f) for name, _, f in path.ops())
+    for name in ops:
+        ops[name]()
+    for name in ("padded_gather", "padded_scatter", "padded_wgrad"):
+        ops[name]()
+    torch.cuda.synchronize(dev)
+    print(json.dumps({"profile_case": r.name, "tokens": r.T, "padded_rows": path.P, "kept": path.kept,
+                      "algorithmic_bytes": path.algorithmic_bytes()}))
+
+
+def main():
+    args = parse()
+    if args.profile_case:
+        run_profile_case(args)
+        return
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        run_reference(args, rank)
+        return
+    run_gpu(args, rank, world, local_rank)
+
+
+if __name__ == "__main__":
+    main()

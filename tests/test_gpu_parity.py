@@ -327,5 +327,6 @@ def test_error_codes_through_the_binding():
     xs = torch.zeros((4, 8), device=DEV)
     with pytest.raises(p.MoeError) as ei:
         p.moe_binned_gather(xs, torch.zeros(8, dtype=torch.int32, device=DEV),
-                            torch.zeros(2, dtype=torch.int32, device=DEV), 2, -1, 2)
+                            torch.zeros(2, dtype=torch.int32, device=DEV), 2, -1, 2,
+                            out=torch.empty((2, 1, 8), device=DEV))
     assert ei.value.code == _lib.MOE_ERR_INVALID_ARG

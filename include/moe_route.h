@@ -111,6 +111,40 @@ int moe_route_build(const int32_t* top_expert, int64_t n, int32_t num_experts,
                     moe_stream_t stream);
 
 /*
+ * Route build that allocates nothing. The pages have no counterpart: this is
+ * a convenience of this library, not part of the method.
+ * Same arguments, outputs and device-status behaviour as moe_route_build,
+ * minus the workspace. It is meant for callers that cannot hand the library
+ * any scratch memory: a plain C host that owns only its inputs and outputs,
+ * a plugin running under a framework that holds the whole device memory pool
+ * without exposing an allocator, or a hot loop that must not call cudaMalloc
+ * (which may synchronise the device).
+ *  - The scratch is a static device array of MOE_ROUTE_BUILD_NOALLOC_MAX_BYTES
+ *    inside the library; every GPU on which the library is loaded keeps it
+ *    reserved until the process exits. No cudaMalloc / cudaFree is called.
+ *  - Size limit: returns MOE_ERR_INVALID_ARG, without enqueuing anything,
+ *    when moe_route_build_workspace_size(n, num_experts) exceeds
+ *    MOE_ROUTE_BUILD_NOALLOC_MAX_BYTES (for E = 256 that is n above about
+ *    two million assignments); use moe_route_build with a caller workspace
+ *    then.
+ *  - The first call on a device looks up the array's device address
+ *    (cudaGetSymbolAddress) and caches it; make that first call before any
+ *    stream capture on that device. It returns MOE_ERR_CUDA if the lookup
+ *    fails.
+ *  - All calls on a device share the one array, which keeps the last call's
+ *    contents (nothing in it needs to start at zero). Calls whose work
+ *    overlaps on the GPU - on different streams without ordering between
+ *    them - race on it and produce wrong results: order them on one stream
+ *    or with events.
+ */
+#define MOE_ROUTE_BUILD_NOALLOC_MAX_BYTES (1u << 20)
+int moe_route_build_noalloc(const int32_t* top_expert, int64_t n,
+                            int32_t num_experts, int32_t pad_multiple,
+                            int32_t* indices, int32_t* bin_ids, int32_t* bins,
+                            int32_t* padded_bins, int32_t* positions,
+                            int32_t* d_status, moe_stream_t stream);
+
+/*
  * Binned gather ([binned] Goal, Workflow step 3, Implementation Pattern,
  * Guardrails). For expert e and slot j < capacity:
  *   out[e, j, :] = x[indices[bins[e-1] + j] / top_k, :]  if j < count_e,

@@ -18,7 +18,7 @@ def lib():
 
 def test_header_and_exports_agree(lib):
     declared = _lib.header_functions()
-    assert len(declared) == len(set(declared)) == 13
+    assert len(declared) == len(set(declared)) == 14
     out = subprocess.run(["nm", "-D", "--defined-only", _lib.LIB_PATH], capture_output=True, text=True,
                          check=True).stdout
     exported = {ln.split()[-1] for ln in out.splitlines() if " T " in ln}

@@ -1,0 +1,61 @@
+"""The route build entry point that allocates nothing.
+
+Some callers cannot give the library scratch memory (a plain C host that
+owns only its inputs and outputs, a plugin under a framework that holds the
+whole device memory pool, a hot loop that must not call cudaMalloc).
+moe_route_build_noalloc serves them from a fixed device array inside the
+library. This test calls it through the C ABI twice in a row, on different
+inputs (so the second call starts from the first call's leftover scratch),
+and checks every output against moe_route_build with a caller workspace: the
+outputs are integer index vectors, so they must agree bit for bit. It also
+checks that a request larger than the fixed array is refused before any work
+is enqueued.
+
+The file is named so that pytest collects it last; it passes alone in a
+fresh process (where its first call also performs the one-time address
+lookup) and after the other tests.
+"""
+import numpy as np
+import pytest
+import torch
+
+from padded_permute_combine_gb300 import _lib, ops
+
+pytestmark = pytest.mark.gpu
+
+
+def _ptr(t):
+    return None if t is None else t.data_ptr()
+
+
+def test_noalloc_route_build_matches_workspace_route_build():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    lib = _lib.load()
+    dev = torch.device("cuda:0")
+    stream = torch.cuda.current_stream(dev).cuda_stream
+    g = np.random.default_rng(2024)
+    # large first, then smaller: the second call sees stale scratch contents
+    for n, E, m in [(65536, 256, 128), (5003, 64, 16)]:
+        p = 1.0 / np.arange(1, E + 1) ** 1.1
+        te_np = g.choice(E, size=n, p=p / p.sum()).astype(np.int32)
+        te = torch.from_numpy(te_np).to(dev)
+        want = ops.moe_route_build(te, E, m)
+        got = [torch.full((n,), -7, dtype=torch.int32, device=dev),
+               torch.full((n,), -7, dtype=torch.int32, device=dev),
+               torch.full((E,), -7, dtype=torch.int32, device=dev),
+               torch.full((E,), -7, dtype=torch.int32, device=dev),
+               torch.full((n,), -7, dtype=torch.int32, device=dev)]
+        status = torch.zeros(1, dtype=torch.int32, device=dev)
+        rc = lib.moe_route_build_noalloc(_ptr(te), n, E, m, *[_ptr(t) for t in got], _ptr(status), stream)
+        assert rc == _lib.MOE_OK, lib.moe_error_string(rc)
+        torch.cuda.synchronize(dev)
+        assert int(status.item()) == 0
+        for name, a, b in zip(("indices", "bin_ids", "bins", "padded_bins", "positions"), got, want):
+            assert torch.equal(a, b), name
+
+    # more scratch than the fixed array holds: refused on the host
+    big_n = 1 << 22
+    assert lib.moe_route_build_workspace_size(big_n, 256) > (1 << 20)
+    rc = lib.moe_route_build_noalloc(_ptr(te), big_n, 256, 1, *[_ptr(t) for t in got], None, stream)
+    assert rc == _lib.MOE_ERR_INVALID_ARG

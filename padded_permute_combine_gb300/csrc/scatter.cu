@@ -8,9 +8,11 @@
 // FMA contraction), then rounds once to the output type. Because every
 // assignment id is unique, each output element has exactly one writer and no
 // atomics are needed. A slot finds its expert row through the inverse
-// permutation `positions`; slots dropped by capacity are skipped. Loads of
-// up to four slots are issued before they are summed, to keep bytes in
-// flight.
+// permutation `positions`; slots dropped by capacity are compacted away
+// (ballot + __fns keeps slot order), and the loads of up to eight kept slots
+// are issued before they are summed, to keep bytes in flight. Sums use
+// Blackwell's packed f32x2 add, still rounding each operation to nearest,
+// so the result is bit-identical to the scalar sequence.
 #include "common.cuh"
 #include "vec_math.cuh"
 
@@ -33,6 +35,7 @@ struct ScatterArgs {
   int64_t seg_vecs;  // vectors per work item
   int64_t segs;      // work items per token
   int64_t xe_rows;
+  bool offsets32;  // every vector index of xe fits in 32 bits
   int32_t E;
   int32_t capacity;
   int32_t top_k;
@@ -60,12 +63,116 @@ __device__ __forceinline__ int64_t slot_row(const ScatterArgs& g, int64_t a) {
   return row;
 }
 
-template <int VB, int U, typename ET, bool PADDED, bool WEIGHTED>
-__global__ void __launch_bounds__(kThreads) scatter_kernel(ScatterArgs g) {
+// Adds the elements of one expert-row vector (scaled when WEIGHTED) to the
+// accumulators, each 64-bit acc2 register holding a pair of fp32 sums. The
+// scaling multiplies are scalar __fmul_rn, which is never merged into a
+// fused multiply-add, so every term is rounded on its own before the
+// (packed, round-to-nearest) add, exactly as in the scalar definition.
+template <typename ET, typename V, int NP, bool WEIGHTED>
+__device__ __forceinline__ void add_vec_packed(uint64_t (&acc2)[NP], const V& v, float w) {
+#pragma unroll
+  for (int p = 0; p < NP; ++p) {
+    const uint64_t x2 = f2_elems<ET>(v, p);
+    if (WEIGHTED) {
+      float lo, hi;
+      f2_unpack(x2, lo, hi);
+      acc2[p] = f2_add(acc2[p], f2_pack(__float_as_uint(__fmul_rn(w, lo)), __float_as_uint(__fmul_rn(w, hi))));
+    } else {
+      acc2[p] = f2_add(acc2[p], x2);
+    }
+  }
+}
+
+template <int VB, typename ET, bool WEIGHTED>
+__device__ __forceinline__ void add_vec_scalar(float (&acc)[Lanes<VB, ET>::kElems],
+                                               const typename Lanes<VB, ET>::V& v, float w) {
+#pragma unroll
+  for (int e = 0; e < Lanes<VB, ET>::kElems; ++e) {
+    const float x = Lanes<VB, ET>::get(v, e);
+    acc[e] = WEIGHTED ? __fadd_rn(acc[e], __fmul_rn(w, x)) : __fadd_rn(acc[e], x);
+  }
+}
+
+// Lane j receives the j-th kept slot (in slot order) of the 32 slots whose
+// rows and weights the lanes hold; returns the number of kept slots.
+__device__ __forceinline__ int compact_kept(int64_t& row, float& w) {
+  const unsigned mask = __ballot_sync(0xffffffffu, row >= 0);
+  const int nk = __popc(mask);
+  const int lane = lane_id();
+  const int src = lane < nk ? (int)__fns(mask, 0, lane + 1) : 0;
+  const int64_t r = __shfl_sync(0xffffffffu, row, src);
+  const float ww = __shfl_sync(0xffffffffu, w, src);
+  row = lane < nk ? r : -1;
+  w = ww;
+  return nk;
+}
+
+// Streams columns [c_begin, c_end) of one output row from nk (<= KQ) kept
+// expert rows held as 32-bit vector offsets, U warp-wide column chunks per
+// pass, so that KQ * U loads per lane are in flight together.
+template <int KQ, int U, int VB, typename ET, bool WEIGHTED>
+__device__ __forceinline__ void stream_kept(const typename Lanes<VB, ET>::V* __restrict__ xe,
+                                            typename Lanes<VB, ET>::V* __restrict__ dst, const uint32_t (&off)[8],
+                                            const float (&w)[8], int nk, int64_t c_begin, int64_t c_end, int lane) {
   using L = Lanes<VB, ET>;
   using V = typename L::V;
   constexpr int NE = L::kElems;
-  constexpr int KG = 4;  // slots whose loads are in flight together
+  constexpr bool kPacked = (NE % 2) == 0;
+  constexpr int NP = kPacked ? NE / 2 : 1;
+  for (int64_t c0 = c_begin; c0 < c_end; c0 += (int64_t)U * kWarp) {
+    V v[KQ][U];
+#pragma unroll
+    for (int q = 0; q < KQ; ++q) {
+      if (q < nk) {
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+          const int64_t c = c0 + u * kWarp + lane;
+          if (c < c_end) v[q][u] = ld_stream(xe + c + off[q]);
+        }
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int64_t c = c0 + u * kWarp + lane;
+      if (c >= c_end) break;
+      float acc[NE];
+      if constexpr (kPacked) {
+        uint64_t acc2[NP];
+#pragma unroll
+        for (int p = 0; p < NP; ++p) acc2[p] = 0ull;
+#pragma unroll
+        for (int q = 0; q < KQ; ++q)
+          if (q < nk) add_vec_packed<ET, V, NP, WEIGHTED>(acc2, v[q][u], w[q]);
+#pragma unroll
+        for (int p = 0; p < NP; ++p) f2_unpack(acc2[p], acc[2 * p], acc[2 * p + 1]);
+      } else {
+#pragma unroll
+        for (int e = 0; e < NE; ++e) acc[e] = 0.0f;
+#pragma unroll
+        for (int q = 0; q < KQ; ++q)
+          if (q < nk) add_vec_scalar<VB, ET, WEIGHTED>(acc, v[q][u], w[q]);
+      }
+      st_stream(dst + c, L::pack(acc));
+    }
+  }
+}
+
+constexpr int kKeptInFlight = 8;  // kept slots whose loads are issued together
+constexpr int kRareGroup = 4;     // slots per group when more than kKeptInFlight are kept
+#ifndef MOE_SCATTER_MIN_BLOCKS
+#define MOE_SCATTER_MIN_BLOCKS 2
+#endif
+constexpr int kMinBlocks = MOE_SCATTER_MIN_BLOCKS;  // CTAs per SM the register budget must allow
+
+template <int VB, typename ET, bool PADDED, bool WEIGHTED>
+__global__ void __launch_bounds__(kThreads, kMinBlocks) scatter_kernel(ScatterArgs g) {
+  using L = Lanes<VB, ET>;
+  using V = typename L::V;
+  constexpr int NE = L::kElems;
+  constexpr bool kPacked = (NE % 2) == 0;
+  constexpr int NP = kPacked ? NE / 2 : 1;
+  constexpr int KR = kKeptInFlight;
+  constexpr int KG = kRareGroup;
   const int lane = lane_id();
   const int64_t warps = (int64_t)gridDim.x * (blockDim.x / kWarp);
   const int64_t items = g.T * g.segs;
@@ -77,7 +184,8 @@ __global__ void __launch_bounds__(kThreads) scatter_kernel(ScatterArgs g) {
     const int64_t t = item / g.segs;
     const int64_t c_begin = (item - t * g.segs) * g.seg_vecs;
     const int64_t c_end = min(c_begin + g.seg_vecs, g.vecs);
-    // Lane k (and k + 32) resolves slot k of this token.
+    // Lane k (and k + 32) resolves slot k of this token, then the kept slots
+    // of each half are compacted to the low lanes, keeping slot order.
     int64_t row_lo = -1, row_hi = -1;
     float w_lo = 1.0f, w_hi = 1.0f;
     if (lane < g.top_k) {
@@ -90,52 +198,62 @@ __global__ void __launch_bounds__(kThreads) scatter_kernel(ScatterArgs g) {
       row_hi = slot_row<PADDED>(g, a);
       if (WEIGHTED) w_hi = __ldg(g.weights + a);
     }
-    for (int64_t c0 = c_begin; c0 < c_end; c0 += kWarp * U) {
-      float acc[U][NE];
-#pragma unroll
-      for (int u = 0; u < U; ++u)
-#pragma unroll
-        for (int q = 0; q < NE; ++q) acc[u][q] = 0.0f;
-      for (int kb = 0; kb < g.top_k; kb += KG) {
-        int64_t r[KG];
-        float w[KG];
-        V v[KG][U];
-#pragma unroll
-        for (int q = 0; q < KG; ++q) {
-          const int k = kb + q;
-          const bool hi = k >= kWarp;
-          r[q] = __shfl_sync(0xffffffffu, hi ? row_hi : row_lo, k & (kWarp - 1));
-          w[q] = __shfl_sync(0xffffffffu, hi ? w_hi : w_lo, k & (kWarp - 1));
-          if (k >= g.top_k) r[q] = -1;
-          if (r[q] >= 0) {
-            const V* src = xe + r[q] * g.vecs;
-#pragma unroll
-            for (int u = 0; u < U; ++u) {
-              const int64_t c = c0 + u * kWarp + lane;
-              if (c < c_end) v[q][u] = ld_stream(src + c);
-            }
-          }
-        }
-#pragma unroll
-        for (int q = 0; q < KG; ++q) {
-          if (r[q] < 0) continue;
-#pragma unroll
-          for (int u = 0; u < U; ++u) {
-            const int64_t c = c0 + u * kWarp + lane;
-            if (c >= c_end) continue;
-#pragma unroll
-            for (int e = 0; e < NE; ++e) {
-              const float x = L::get(v[q][u], e);
-              acc[u][e] = WEIGHTED ? __fadd_rn(acc[u][e], __fmul_rn(w[q], x)) : __fadd_rn(acc[u][e], x);
-            }
-          }
-        }
+    int n_lo = compact_kept(row_lo, w_lo);
+    int n_hi = g.top_k > kWarp ? compact_kept(row_hi, w_hi) : 0;
+    if (n_hi > 0 && n_lo + n_hi <= kWarp) {
+      // Append the kept upper-half slots after the lower-half ones.
+      const int src = (lane - n_lo) & (kWarp - 1);
+      const int64_t rh = __shfl_sync(0xffffffffu, row_hi, src);
+      const float wh = __shfl_sync(0xffffffffu, w_hi, src);
+      if (lane >= n_lo && lane < n_lo + n_hi) {
+        row_lo = rh;
+        w_lo = wh;
       }
-      V* dst = out + t * g.vecs;
+      n_lo += n_hi;
+      n_hi = 0;
+    }
+    V* dst = out + t * g.vecs;
+    if (g.offsets32 && n_hi == 0 && n_lo <= KR) {
+      // Common case: every kept row stays in registers (as a 32-bit vector
+      // offset into xe) for the whole segment, and all their loads are in
+      // flight together.
+      uint32_t off0[KR];
+      float w0[KR];
 #pragma unroll
-      for (int u = 0; u < U; ++u) {
-        const int64_t c = c0 + u * kWarp + lane;
-        if (c < c_end) st_stream(dst + c, L::pack(acc[u]));
+      for (int q = 0; q < KR; ++q) {
+        const int64_t r = __shfl_sync(0xffffffffu, row_lo, q);
+        off0[q] = (uint32_t)((r < 0 ? 0 : r) * g.vecs);
+        w0[q] = __shfl_sync(0xffffffffu, w_lo, q);
+      }
+      // Fewer kept rows leave room for more column chunks per pass.
+      if (n_lo > 4) stream_kept<8, 1, VB, ET, WEIGHTED>(xe, dst, off0, w0, n_lo, c_begin, c_end, lane);
+      else stream_kept<4, 2, VB, ET, WEIGHTED>(xe, dst, off0, w0, n_lo, c_begin, c_end, lane);
+    } else {
+      // More than KR kept slots (large TOP_K): groups of KG, low half first,
+      // rows fetched from the compacted lanes on every pass.
+      for (int64_t c0 = c_begin; c0 < c_end; c0 += kWarp) {
+        const int64_t c = c0 + lane;
+        const bool in = c < c_end;
+        float acc[NE];
+#pragma unroll
+        for (int e = 0; e < NE; ++e) acc[e] = 0.0f;
+        for (int h = 0; h < 2; ++h) {
+          const int nh = h == 0 ? n_lo : n_hi;
+          for (int g0 = 0; g0 < nh; g0 += KG) {
+            V v[KG];
+            float wq[KG];
+#pragma unroll
+            for (int q = 0; q < KG; ++q) {
+              const int64_t r = __shfl_sync(0xffffffffu, h == 0 ? row_lo : row_hi, (g0 + q) & (kWarp - 1));
+              wq[q] = __shfl_sync(0xffffffffu, h == 0 ? w_lo : w_hi, (g0 + q) & (kWarp - 1));
+              if (g0 + q < nh && in) v[q] = ld_stream(xe + r * g.vecs + c);
+            }
+#pragma unroll
+            for (int q = 0; q < KG; ++q)
+              if (g0 + q < nh && in) add_vec_scalar<VB, ET, WEIGHTED>(acc, v[q], wq[q]);
+          }
+        }
+        if (in) st_stream(dst + c, L::pack(acc));
       }
     }
   }
@@ -152,15 +270,17 @@ __global__ void invert_kernel(const int32_t* __restrict__ indices, int64_t n, in
 
 template <int VB, typename ET, bool PADDED>
 int launch_scatter(ScatterArgs g, cudaStream_t s) {
-  constexpr int U = (VB == 16) ? 2 : 4;
-  g.seg_vecs = (int64_t)kWarp * U * 2;
+  // Column segments of at most 256 vectors, rounded to whole warp passes.
+  g.segs = (g.vecs + 255) / 256;
+  g.seg_vecs = ((g.vecs + g.segs - 1) / g.segs + kWarp - 1) / kWarp * kWarp;
   g.segs = (g.vecs + g.seg_vecs - 1) / g.seg_vecs;
+  g.offsets32 = (uint64_t)g.xe_rows * (uint64_t)g.vecs <= 0xffffffffull;
   const int64_t work_ctas = (g.T * g.segs + (kThreads / kWarp) - 1) / (kThreads / kWarp);
   if (g.weights != nullptr) {
-    auto k = scatter_kernel<VB, U, ET, PADDED, true>;
+    auto k = scatter_kernel<VB, ET, PADDED, true>;
     k<<<persistent_grid(k, kThreads, 0, work_ctas), kThreads, 0, s>>>(g);
   } else {
-    auto k = scatter_kernel<VB, U, ET, PADDED, false>;
+    auto k = scatter_kernel<VB, ET, PADDED, false>;
     k<<<persistent_grid(k, kThreads, 0, work_ctas), kThreads, 0, s>>>(g);
   }
   return check_launch();
@@ -237,7 +357,7 @@ extern "C" int moe_binned_scatter(const void* xe, int32_t dtype, const int32_t* 
   if (T == 0 || H == 0) return MOE_OK;
   if (xe == nullptr && capacity > 0) return MOE_ERR_INVALID_ARG;
   ScatterArgs g{static_cast<const char*>(xe), static_cast<char*>(out), bin_ids, bins, nullptr, weights, positions,
-                T, T * top_k, H, 0, 0, (int64_t)E * capacity, E, capacity, top_k, d_status};
+                T, T * top_k, H, 0, 0, (int64_t)E * capacity, false, E, capacity, top_k, d_status};
   return run_scatter<false>(g, dtype, indices, workspace, workspace_bytes, reinterpret_cast<cudaStream_t>(stream));
 }
 
@@ -253,6 +373,6 @@ extern "C" int moe_padded_scatter(const void* xe, int32_t dtype, const int32_t* 
   if (T == 0 || H == 0) return MOE_OK;
   if (xe == nullptr && xe_rows > 0) return MOE_ERR_INVALID_ARG;
   ScatterArgs g{static_cast<const char*>(xe), static_cast<char*>(out), bin_ids, bins, padded_bins, weights,
-                positions, T, T * top_k, H, 0, 0, xe_rows, E, 0, top_k, d_status};
+                positions, T, T * top_k, H, 0, 0, xe_rows, false, E, 0, top_k, d_status};
   return run_scatter<true>(g, dtype, indices, workspace, workspace_bytes, reinterpret_cast<cudaStream_t>(stream));
 }

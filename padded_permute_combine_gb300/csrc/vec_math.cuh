@@ -63,3 +63,48 @@ template <> struct Lanes<2, __nv_bfloat16> {
 };
 
 }  // namespace moe
+
+namespace moe {
+
+// Two fp32 values in one 64-bit register, operated on by Blackwell's packed
+// f32x2 instructions (each half rounded to nearest, like __fadd_rn /
+// __fmul_rn; subnormals kept).
+__device__ __forceinline__ uint64_t f2_pack(uint32_t lo, uint32_t hi) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1,%2};" : "=l"(r) : "r"(lo), "r"(hi));
+  return r;
+}
+__device__ __forceinline__ void f2_unpack(uint64_t v, float& lo, float& hi) {
+  uint32_t a, b;
+  asm("mov.b64 {%0,%1}, %2;" : "=r"(a), "=r"(b) : "l"(v));
+  lo = __uint_as_float(a);
+  hi = __uint_as_float(b);
+}
+__device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ uint64_t f2_sub(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ uint64_t f2_mul(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+// Word q of a vector as an fp32 pair: two bf16 elements (low first) or, for
+// fp32 rows, elements 2q and 2q+1.
+template <typename ET, typename V>
+__device__ __forceinline__ uint64_t f2_elems(const V& v, int q) {
+  if constexpr (Elem<ET>::kBytes == 2) {
+    const uint32_t w = Words<V>::get(v, q);
+    return f2_pack(w << 16, w & 0xffff0000u);
+  } else {
+    return f2_pack(Words<V>::get(v, 2 * q), Words<V>::get(v, 2 * q + 1));
+  }
+}
+
+}  // namespace moe

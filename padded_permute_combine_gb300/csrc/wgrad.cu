@@ -11,7 +11,9 @@
 // Sci. Comput. 26(6), 2005, algorithm Dot2): every product and every partial
 // sum carries its exact rounding error (TwoProduct via fma, Knuth's TwoSum),
 // the errors are summed separately and added once at the end, and the warp
-// reduction combines (sum, error) pairs the same way. The result is as
+// reduction combines (sum, error) pairs the same way. For bf16 rows the
+// products are exact and the running sums use packed f32x2 instructions, two
+// independent compensated sums per register. The result is as
 // accurate as a dot computed in twice the working precision and then
 // rounded, independent of H. A dropped position writes 0. Every wgrad entry
 // is written by exactly one warp because indices is a permutation.
@@ -64,6 +66,27 @@ struct Acc2 {
   }
 };
 
+// Two running compensated sums in the halves of packed f32x2 registers.
+// Used for bf16 rows, whose products are exact in fp32 (8-bit x 8-bit
+// significands), so only the sums carry rounding errors.
+struct Acc2x2 {
+  uint64_t s = 0ull, c = 0ull;
+  __device__ __forceinline__ void add_exact(uint64_t p) {
+    const uint64_t t = f2_add(s, p);
+    const uint64_t bb = f2_sub(t, s);
+    const uint64_t e = f2_add(f2_sub(s, f2_sub(t, bb)), f2_sub(p, bb));
+    s = t;
+    c = f2_add(c, e);
+  }
+  __device__ __forceinline__ void fold_into(Acc2& a) const {
+    float s0, s1, c0, c1;
+    f2_unpack(s, s0, s1);
+    f2_unpack(c, c0, c1);
+    a.merge(s0, c0);
+    a.merge(s1, c1);
+  }
+};
+
 template <int VB, int U, typename ET, bool PADDED>
 __global__ void __launch_bounds__(kThreads) wgrad_kernel(WgradArgs g) {
   using L = Lanes<VB, ET>;
@@ -106,7 +129,9 @@ __global__ void __launch_bounds__(kThreads) wgrad_kernel(WgradArgs g) {
     }
     const V* xr = xe + row * g.vecs;
     const V* gv = gr + (int64_t)(a / g.top_k) * g.vecs;
+    constexpr bool kPacked = kExact && NE % 2 == 0;
     Acc2 acc[2];
+    Acc2x2 acc2[2];
     for (int64_t c0 = 0; c0 < g.vecs; c0 += kWarp * U) {
       V vx[U], vg[U];
 #pragma unroll
@@ -121,10 +146,20 @@ __global__ void __launch_bounds__(kThreads) wgrad_kernel(WgradArgs g) {
       for (int u = 0; u < U; ++u) {
         const int64_t c = c0 + u * kWarp + lane;
         if (c < g.vecs) {
+          if constexpr (kPacked) {
 #pragma unroll
-          for (int q = 0; q < NE; ++q) acc[q & 1].template add_product<kExact>(L::get(vx[u], q), L::get(vg[u], q));
+            for (int p = 0; p < NE / 2; ++p)
+              acc2[p & 1].add_exact(f2_mul(f2_elems<ET>(vx[u], p), f2_elems<ET>(vg[u], p)));
+          } else {
+#pragma unroll
+            for (int q = 0; q < NE; ++q) acc[q & 1].template add_product<kExact>(L::get(vx[u], q), L::get(vg[u], q));
+          }
         }
       }
+    }
+    if constexpr (kPacked) {
+      acc2[0].fold_into(acc[0]);
+      acc2[1].fold_into(acc[1]);
     }
     acc[0].merge(acc[1].s, acc[1].c);
 #pragma unroll

@@ -171,6 +171,13 @@ def test_top_k_values(K):
     run_routing(r)
 
 
+@pytest.mark.parametrize("cap", [1, 2, 3, 8, 40])
+def test_large_top_k_kept_mixes(cap):
+    # K > 32: kept slots in both halves, totals on both sides of eight
+    r = wl.uniform_routing("k36-cap%d" % cap, 31, 40, 44, 36, wl.F32, capacity=cap, pad_multiple=4, seed=cap)
+    run_routing(r, padded=(cap == 40))
+
+
 def test_capacity_edges():
     base = wl.zipf_routing("cap", 300, 40, 16, 4, wl.F32, pad_multiple=3, seed=5)
     maxc = int(np.bincount(base.top_expert.reshape(-1), minlength=16).max())

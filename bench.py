@@ -55,6 +55,8 @@ def parse():
     ap.add_argument("--profile-case", action="store_true",
                     help="no timing: run each op of a smaller batch twice, for an ncu capture")
     ap.add_argument("--tokens", type=int, default=4096, help="tokens of the --profile-case batch")
+    ap.add_argument("--profile-ops", default="padded_gather,padded_scatter,padded_wgrad",
+                    help="ops the --profile-case runs a second time, in this order")
     a = ap.parse_args()
     a.warmup = max(3, a.warmup)
     a.steps = max(1, a.steps)
@@ -496,9 +498,10 @@ def run_reference(args, rank):
 
 
 def run_profile_case(args):
-    """Each op of a `--tokens`-token batch once as warm-up, then the padded
-    gather, scatter and wgrad once more: three launches for `ncu -s 3 -c 3`
-    on the gather/scatter/wgrad kernels."""
+    """Each op of a `--tokens`-token batch once as warm-up, then the ops of
+    `--profile-ops` once more. With `ncu -k regex:"gather_kernel|
+    scatter_kernel|wgrad_kernel" -s 8` the captured launches are exactly
+    that second pass (the set-up and warm-up launch eight matching kernels)."""
     import torch
 
     dev = torch.device("cuda", 0)
@@ -507,7 +510,7 @@ def run_profile_case(args):
     ops = dict((name, f) for name, _, f in path.ops())
     for name in ops:
         ops[name]()
-    for name in ("padded_gather", "padded_scatter", "padded_wgrad"):
+    for name in args.profile_ops.split(","):
         ops[name]()
     torch.cuda.synchronize(dev)
     print(json.dumps({"profile_case": r.name, "tokens": r.T, "padded_rows": path.P, "kept": path.kept,

@@ -25,14 +25,28 @@ __device__ __forceinline__ unsigned lanemask_lt() {
   return m;
 }
 
+// 32 bytes moved by one 256-bit load or store (sm_100 and later).
+struct alignas(32) u32x8 {
+  uint32_t w[8];
+};
+
 // Vector of VB bytes used for row copies.
 template <int VB> struct Vec;
+template <> struct Vec<32> { using T = u32x8; };
 template <> struct Vec<16> { using T = uint4; };
 template <> struct Vec<8> { using T = uint2; };
 template <> struct Vec<4> { using T = uint32_t; };
 template <> struct Vec<2> { using T = uint16_t; };
 
 // Read-only load of data that is not re-read through L1.
+__device__ __forceinline__ u32x8 ld_stream(const u32x8* p) {
+  u32x8 v;
+  asm volatile("ld.global.nc.L1::no_allocate.v8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+               : "=r"(v.w[0]), "=r"(v.w[1]), "=r"(v.w[2]), "=r"(v.w[3]), "=r"(v.w[4]), "=r"(v.w[5]), "=r"(v.w[6]),
+                 "=r"(v.w[7])
+               : "l"(p));
+  return v;
+}
 __device__ __forceinline__ uint4 ld_stream(const uint4* p) {
   uint4 v;
   asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
@@ -56,6 +70,11 @@ __device__ __forceinline__ uint16_t ld_stream(const uint16_t* p) {
 }
 
 // Store of write-once output: evict-first so it does not push reused inputs out of L2.
+__device__ __forceinline__ void st_stream(u32x8* p, const u32x8& v) {
+  asm volatile("st.global.cs.v8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"l"(p), "r"(v.w[0]), "r"(v.w[1]),
+               "r"(v.w[2]), "r"(v.w[3]), "r"(v.w[4]), "r"(v.w[5]), "r"(v.w[6]), "r"(v.w[7])
+               : "memory");
+}
 __device__ __forceinline__ void st_stream(uint4* p, uint4 v) {
   asm volatile("st.global.cs.v4.u32 [%0], {%1,%2,%3,%4};" ::"l"(p), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
                : "memory");
@@ -71,6 +90,12 @@ __device__ __forceinline__ void st_stream(uint16_t* p, uint16_t v) {
 }
 
 template <typename V> __device__ __forceinline__ V zero_vec();
+template <> __device__ __forceinline__ u32x8 zero_vec<u32x8>() {
+  u32x8 v;
+#pragma unroll
+  for (int q = 0; q < 8; ++q) v.w[q] = 0u;
+  return v;
+}
 template <> __device__ __forceinline__ uint4 zero_vec<uint4>() { return make_uint4(0, 0, 0, 0); }
 template <> __device__ __forceinline__ uint2 zero_vec<uint2>() { return make_uint2(0, 0); }
 template <> __device__ __forceinline__ uint32_t zero_vec<uint32_t>() { return 0u; }
@@ -110,10 +135,10 @@ int check_launch();  // MOE_OK or MOE_ERR_CUDA after a launch
 inline bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 inline int dtype_bytes(int32_t dtype) { return dtype == MOE_F32 ? 4 : (dtype == MOE_BF16 ? 2 : 0); }
 
-// Widest vector (16, 8, 4 or 2 bytes, at least min_bytes) that divides the
-// row and keeps every given pointer aligned; 0 if none.
-inline int pick_vec_bytes(int64_t row_bytes, const void* const* ptrs, int nptrs, int min_bytes) {
-  for (int vb = 16; vb >= min_bytes; vb >>= 1) {
+// Widest vector (max_bytes, ..., 4 or 2 bytes, at least min_bytes) that
+// divides the row and keeps every given pointer aligned; 0 if none.
+inline int pick_vec_bytes(int64_t row_bytes, const void* const* ptrs, int nptrs, int min_bytes, int max_bytes = 16) {
+  for (int vb = max_bytes; vb >= min_bytes; vb >>= 1) {
     if (row_bytes % vb) continue;
     bool ok = true;
     for (int q = 0; q < nptrs; ++q) ok = ok && (ptrs[q] == nullptr || aligned(ptrs[q], vb));

@@ -7,7 +7,8 @@
 // Destination-major: every output row is produced exactly once, either as a
 // copy of its source token row or as zeros (unused capacity / padding), so no
 // separate clearing pass is needed. One warp owns one output row at a time
-// and streams it with VB-byte vectors, U vectors per lane in flight. The bin
+// and streams it with VB-byte vectors (256-bit loads and stores when the row
+// and pointers allow), U vectors per lane in flight. The bin
 // vectors are staged in shared memory; a padded row finds its expert by
 // binary search over padded_bins.
 #include "common.cuh"
@@ -125,7 +126,7 @@ __global__ void __launch_bounds__(kThreads) gather_kernel(GatherArgs g) {
 
 template <int VB, bool PADDED>
 int launch_gather(const GatherArgs& g, cudaStream_t s) {
-  constexpr int U = VB >= 8 ? 8 : 16;
+  constexpr int U = VB == 32 ? 4 : (VB >= 8 ? 8 : 16);  // 128 bytes per lane in flight
   auto k = gather_kernel<VB, U, PADDED>;
   const int64_t work_ctas = (g.rows_out + (kThreads / kWarp) - 1) / (kThreads / kWarp);
   const int grid = persistent_grid(k, kThreads, 0, work_ctas);
@@ -137,10 +138,11 @@ template <bool PADDED>
 int dispatch_gather(GatherArgs g, int elem, const void* x, void* out, cudaStream_t s) {
   const int64_t row_bytes = g.vecs * elem;  // g.vecs holds H on entry
   const void* ptrs[] = {x, out};
-  const int vb = pick_vec_bytes(row_bytes, ptrs, 2, elem);
+  const int vb = pick_vec_bytes(row_bytes, ptrs, 2, elem, 32);
   if (vb == 0) return MOE_ERR_UNSUPPORTED;
   g.vecs = row_bytes / vb;
   switch (vb) {
+    case 32: return launch_gather<32, PADDED>(g, s);
     case 16: return launch_gather<16, PADDED>(g, s);
     case 8: return launch_gather<8, PADDED>(g, s);
     case 4: return launch_gather<4, PADDED>(g, s);

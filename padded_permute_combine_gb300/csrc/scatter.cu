@@ -107,53 +107,75 @@ __device__ __forceinline__ int compact_kept(int64_t& row, float& w) {
   return nk;
 }
 
-// Streams columns [c_begin, c_end) of one output row from nk (<= KQ) kept
-// expert rows held as 32-bit vector offsets, U warp-wide column chunks per
-// pass, so that KQ * U loads per lane are in flight together.
-template <int KQ, int U, int VB, typename ET, bool WEIGHTED>
-__device__ __forceinline__ void stream_kept(const typename Lanes<VB, ET>::V* __restrict__ xe,
-                                            typename Lanes<VB, ET>::V* __restrict__ dst, const uint32_t (&off)[8],
-                                            const float (&w)[8], int nk, int64_t c_begin, int64_t c_end, int lane) {
+// Sum of the nk kept rows' vectors held in v, stored at dst + c.
+template <int KQ, int VB, typename ET, bool WEIGHTED>
+__device__ __forceinline__ void sum_store(const typename Lanes<VB, ET>::V (&v)[KQ], const float (&w)[8], int nk,
+                                          typename Lanes<VB, ET>::V* dst) {
   using L = Lanes<VB, ET>;
   using V = typename L::V;
   constexpr int NE = L::kElems;
   constexpr bool kPacked = (NE % 2) == 0;
   constexpr int NP = kPacked ? NE / 2 : 1;
-  for (int64_t c0 = c_begin; c0 < c_end; c0 += (int64_t)U * kWarp) {
-    V v[KQ][U];
+  float acc[NE];
+  if constexpr (kPacked) {
+    uint64_t acc2[NP];
 #pragma unroll
-    for (int q = 0; q < KQ; ++q) {
-      if (q < nk) {
+    for (int p = 0; p < NP; ++p) acc2[p] = 0ull;
 #pragma unroll
-        for (int u = 0; u < U; ++u) {
-          const int64_t c = c0 + u * kWarp + lane;
-          if (c < c_end) v[q][u] = ld_stream(xe + c + off[q]);
-        }
-      }
+    for (int q = 0; q < KQ; ++q)
+      if (q < nk) add_vec_packed<ET, V, NP, WEIGHTED>(acc2, v[q], w[q]);
+#pragma unroll
+    for (int p = 0; p < NP; ++p) f2_unpack(acc2[p], acc[2 * p], acc[2 * p + 1]);
+  } else {
+#pragma unroll
+    for (int e = 0; e < NE; ++e) acc[e] = 0.0f;
+#pragma unroll
+    for (int q = 0; q < KQ; ++q)
+      if (q < nk) add_vec_scalar<VB, ET, WEIGHTED>(acc, v[q], w[q]);
+  }
+  st_stream(dst, L::pack(acc));
+}
+
+// Streams columns [c_begin, c_end) of one output row from nk (<= KQ) kept
+// expert rows held as 32-bit vector offsets, one warp-wide chunk per pass.
+// When the registers allow, the passes are software-pipelined over two
+// buffers: the loads of the next chunk are issued before the current chunk
+// is summed, so each lane keeps up to 2 * nk loads in flight.
+template <int KQ, int VB, typename ET, bool WEIGHTED>
+__device__ __forceinline__ void stream_kept(const typename Lanes<VB, ET>::V* __restrict__ xe,
+                                            typename Lanes<VB, ET>::V* __restrict__ dst, const uint32_t (&off)[8],
+                                            const float (&w)[8], int nk, int64_t c_begin, int64_t c_end, int lane) {
+  using V = typename Lanes<VB, ET>::V;
+  if constexpr (KQ * VB > 64) {
+    // Eight wide rows already fill the register budget: no second buffer.
+    for (int64_t c = c_begin + lane; c - lane < c_end; c += kWarp) {
+      V a[KQ];
+#pragma unroll
+      for (int q = 0; q < KQ; ++q)
+        if (q < nk && c < c_end) a[q] = ld_stream(xe + c + off[q]);
+      if (c < c_end) sum_store<KQ, VB, ET, WEIGHTED>(a, w, nk, dst + c);
     }
+    return;
+  }
+  V a[KQ], b[KQ];
+  int64_t c = c_begin + lane;
 #pragma unroll
-    for (int u = 0; u < U; ++u) {
-      const int64_t c = c0 + u * kWarp + lane;
-      if (c >= c_end) break;
-      float acc[NE];
-      if constexpr (kPacked) {
-        uint64_t acc2[NP];
+  for (int q = 0; q < KQ; ++q)
+    if (q < nk && c < c_end) a[q] = ld_stream(xe + c + off[q]);
+  while (c - lane < c_end) {
+    const int64_t cn = c + kWarp;
 #pragma unroll
-        for (int p = 0; p < NP; ++p) acc2[p] = 0ull;
+    for (int q = 0; q < KQ; ++q)
+      if (q < nk && cn < c_end) b[q] = ld_stream(xe + cn + off[q]);
+    if (c < c_end) sum_store<KQ, VB, ET, WEIGHTED>(a, w, nk, dst + c);
+    c = cn;
+    if (c - lane >= c_end) break;
+    const int64_t cm = c + kWarp;
 #pragma unroll
-        for (int q = 0; q < KQ; ++q)
-          if (q < nk) add_vec_packed<ET, V, NP, WEIGHTED>(acc2, v[q][u], w[q]);
-#pragma unroll
-        for (int p = 0; p < NP; ++p) f2_unpack(acc2[p], acc[2 * p], acc[2 * p + 1]);
-      } else {
-#pragma unroll
-        for (int e = 0; e < NE; ++e) acc[e] = 0.0f;
-#pragma unroll
-        for (int q = 0; q < KQ; ++q)
-          if (q < nk) add_vec_scalar<VB, ET, WEIGHTED>(acc, v[q][u], w[q]);
-      }
-      st_stream(dst + c, L::pack(acc));
-    }
+    for (int q = 0; q < KQ; ++q)
+      if (q < nk && cm < c_end) a[q] = ld_stream(xe + cm + off[q]);
+    if (c < c_end) sum_store<KQ, VB, ET, WEIGHTED>(b, w, nk, dst + c);
+    c = cm;
   }
 }
 
@@ -163,6 +185,7 @@ constexpr int kRareGroup = 4;     // slots per group when more than kKeptInFligh
 #define MOE_SCATTER_MIN_BLOCKS 2
 #endif
 constexpr int kMinBlocks = MOE_SCATTER_MIN_BLOCKS;  // CTAs per SM the register budget must allow
+constexpr int64_t kSegTarget = 256;  // vectors per work item, at most
 
 template <int VB, typename ET, bool PADDED, bool WEIGHTED>
 __global__ void __launch_bounds__(kThreads, kMinBlocks) scatter_kernel(ScatterArgs g) {
@@ -225,9 +248,8 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) scatter_kernel(ScatterAr
         off0[q] = (uint32_t)((r < 0 ? 0 : r) * g.vecs);
         w0[q] = __shfl_sync(0xffffffffu, w_lo, q);
       }
-      // Fewer kept rows leave room for more column chunks per pass.
-      if (n_lo > 4) stream_kept<8, 1, VB, ET, WEIGHTED>(xe, dst, off0, w0, n_lo, c_begin, c_end, lane);
-      else stream_kept<4, 2, VB, ET, WEIGHTED>(xe, dst, off0, w0, n_lo, c_begin, c_end, lane);
+      if (n_lo > 4) stream_kept<8, VB, ET, WEIGHTED>(xe, dst, off0, w0, n_lo, c_begin, c_end, lane);
+      else stream_kept<4, VB, ET, WEIGHTED>(xe, dst, off0, w0, n_lo, c_begin, c_end, lane);
     } else {
       // More than KR kept slots (large TOP_K): groups of KG, low half first,
       // rows fetched from the compacted lanes on every pass.
@@ -270,8 +292,8 @@ __global__ void invert_kernel(const int32_t* __restrict__ indices, int64_t n, in
 
 template <int VB, typename ET, bool PADDED>
 int launch_scatter(ScatterArgs g, cudaStream_t s) {
-  // Column segments of at most 256 vectors, rounded to whole warp passes.
-  g.segs = (g.vecs + 255) / 256;
+  // Column segments of at most kSegTarget vectors, rounded to whole warp passes.
+  g.segs = (g.vecs + kSegTarget - 1) / kSegTarget;
   g.seg_vecs = ((g.vecs + g.segs - 1) / g.segs + kWarp - 1) / kWarp * kWarp;
   g.segs = (g.vecs + g.seg_vecs - 1) / g.seg_vecs;
   g.offsets32 = (uint64_t)g.xe_rows * (uint64_t)g.vecs <= 0xffffffffull;

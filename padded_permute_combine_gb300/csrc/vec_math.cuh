@@ -7,6 +7,11 @@ namespace moe {
 
 // 32-bit words of a vector.
 template <typename V> struct Words;
+template <> struct Words<u32x8> {
+  static constexpr int N = 8;
+  __device__ __forceinline__ static uint32_t get(const u32x8& v, int i) { return v.w[i]; }
+  __device__ __forceinline__ static void set(u32x8& v, int i, uint32_t w) { v.w[i] = w; }
+};
 template <> struct Words<uint4> {
   static constexpr int N = 4;
   __device__ __forceinline__ static uint32_t get(const uint4& v, int i) {

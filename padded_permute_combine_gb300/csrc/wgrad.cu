@@ -174,7 +174,7 @@ __global__ void __launch_bounds__(kThreads) wgrad_kernel(WgradArgs g) {
 
 template <int VB, typename ET, bool PADDED>
 int launch_wgrad(const WgradArgs& g, cudaStream_t s) {
-  constexpr int U = (VB == 16) ? 4 : 8;
+  constexpr int U = VB == 32 ? 2 : (VB == 16 ? 4 : 8);  // 64 bytes per lane and operand in flight
   auto k = wgrad_kernel<VB, U, ET, PADDED>;
   const int64_t work_ctas = (g.n + (kThreads / kWarp) - 1) / (kThreads / kWarp);
   k<<<persistent_grid(k, kThreads, 0, work_ctas), kThreads, 0, s>>>(g);
@@ -186,17 +186,19 @@ int run_wgrad(WgradArgs g, int32_t dtype, cudaStream_t s) {
   const int eb = dtype_bytes(dtype);
   const int64_t row_bytes = g.vecs * eb;  // g.vecs holds H on entry
   const void* ptrs[] = {g.xe, g.grad};
-  const int vb = pick_vec_bytes(row_bytes, ptrs, 2, eb);
+  const int vb = pick_vec_bytes(row_bytes, ptrs, 2, eb, 32);
   if (vb == 0) return MOE_ERR_UNSUPPORTED;
   g.vecs = row_bytes / vb;
   if (dtype == MOE_F32) {
     switch (vb) {
+      case 32: return launch_wgrad<32, float, PADDED>(g, s);
       case 16: return launch_wgrad<16, float, PADDED>(g, s);
       case 8: return launch_wgrad<8, float, PADDED>(g, s);
       default: return launch_wgrad<4, float, PADDED>(g, s);
     }
   }
   switch (vb) {
+    case 32: return launch_wgrad<32, __nv_bfloat16, PADDED>(g, s);
     case 16: return launch_wgrad<16, __nv_bfloat16, PADDED>(g, s);
     case 8: return launch_wgrad<8, __nv_bfloat16, PADDED>(g, s);
     case 4: return launch_wgrad<4, __nv_bfloat16, PADDED>(g, s);

@@ -104,6 +104,28 @@ def traffic_from_profiles(kernel: str, digest: str):
     return None
 
 
+def max_over_ranks(x: float, dist, device) -> float:
+    """Largest value of x over all ranks (x itself without a process group).
+    The only collective of the benchmark: timing, never routed data."""
+    if dist is None:
+        return float(x)
+    import torch
+
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def weak_scaling_value(world: int, rows_per_step: int, steps: int, total_ms: float) -> float:
+    """Whole-job rows/s: every rank routes its own batch of rows_per_step."""
+    return world * rows_per_step * steps / (total_ms / 1e3)
+
+
+def rank_workload(rank: int):
+    """Rank r routes its own batch: the same shapes, seed r."""
+    return workload(seed=rank)
+
+
 # ------------------------------------------------------------------ GPU arm
 
 class Path:
@@ -268,7 +290,7 @@ def run_gpu(args, rank, world, local_rank):
         import torch.distributed as dist
 
         dist.init_process_group("nccl", device_id=dev)
-    r, d = workload(seed=rank)
+    r, d = rank_workload(rank)
     path = Path(r, d, dev)
     ops = path.ops()
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.int32, device=dev)
@@ -303,11 +325,7 @@ def run_gpu(args, rank, world, local_rank):
         step_ms.append(ev[s][0].elapsed_time(ev[s][-1]))
         for q, (name, _, _) in enumerate(ops):
             per_kernel[name].append(ev[s][q].elapsed_time(ev[s][q + 1]))
-    total_ms = float(sum(step_ms))
-    if dist is not None:
-        t = torch.tensor([total_ms], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = max_over_ranks(float(sum(step_ms)), dist, dev)
 
     e2e = run_e2e(args, path, dev, dist)
 
@@ -318,7 +336,7 @@ def run_gpu(args, rank, world, local_rank):
         return
     n = path.n
     ms_per_step = total_ms / args.steps
-    value = world * n * args.steps / (total_ms / 1e3)
+    value = weak_scaling_value(world, n, args.steps, total_ms)
     peak, peak_kind = measured_peak()
     algo = path.algorithmic_bytes()
     kern = {}
@@ -409,15 +427,11 @@ def run_e2e(args, path, dev, dist):
         step()
     t1.record(stream)
     torch.cuda.synchronize(dev)
-    ms = t0.elapsed_time(t1)
-    if dist is not None:
-        t = torch.tensor([ms], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(t0.elapsed_time(t1), dist, dev)
     world = dist.get_world_size() if dist is not None else 1
     h2d = sum(v.numel() * v.element_size() for v in h_in.values())
     d2h = sum(v.numel() * v.element_size() for v in h_out.values()) + 4
-    return {"value": round(world * path.n * steps / (ms * 1e-3), 1), "unit": UNIT, "steps": steps,
+    return {"value": round(weak_scaling_value(world, path.n, steps, ms), 1), "unit": UNIT, "steps": steps,
             "ms_per_step": round(ms / steps, 5), "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
 
 

@@ -312,6 +312,14 @@ def check_bf16_rounding(lib):
     assert np.isnan(oracle.to_f32(nan))[0]
 
 
+def check_bf16_golden(lib):
+    """Hand-worked round-to-nearest-even cases (tests/golden/bf16_rounding.txt)."""
+    cases = read_golden("bf16_rounding.txt")["cases"]
+    src = np.array([c[0] for c in cases], np.uint32).view(np.float32)
+    got = oracle.f32_to_bf16(src, lib=lib)
+    assert got.tolist() == [c[1] for c in cases]
+
+
 def read_golden(name):
     """Parse ``key = python-literal`` lines; ``#`` starts a comment."""
     out = {}
@@ -375,4 +383,5 @@ ALL_CHECKS = [
     check_compaction,
     check_bruteforce,
     check_bf16_rounding,
+    check_bf16_golden,
 ]

@@ -2,10 +2,12 @@
 // (Megatron-Core API docs, core.transformer.moe.megakernel.mok.route_adapter:
 //  RoutingMapToIndices forward / backward, routing_map_to_mok_inputs).
 //
-// Forward: one thread per token row. The row of the int8 map is read in
-// 16-byte vectors; __vcmpne4 turns each word into a nonzero-byte mask, and
-// the set bits are walked in increasing expert order until topk routes are
-// emitted; the rest of the row is padded with -1 / 0.0f.
+// Forward: one warp per token row. Each lane reads a few consecutive bytes
+// of the int8 map (one vector load), __vcmpne4 turns them into a
+// nonzero-byte mask, and a warp prefix sum of the per-lane counts gives
+// each route its output slot in increasing expert order; the first topk are
+// emitted with their probabilities and the rest of the row is padded with
+// -1 / 0.0f.
 // Backward: one thread per group of four dense outputs, so the dense
 // gradient is written with full-width coalesced stores; each thread scans the
 // row's topk compact slots (cached in L1) for indices that fall in its group.
@@ -22,39 +24,69 @@ __device__ __forceinline__ unsigned nonzero_bytes(uint32_t w) {
   return ((m >> 7) | (m >> 14) | (m >> 21) | (m >> 28)) & 0xFu;
 }
 
-template <bool VEC16>
+// Nonzero-byte mask of the C bytes of a map row a lane owns (C = 1, 2, 4,
+// 8 or 16 with an aligned row; otherwise bytes one at a time).
+template <int C>
+__device__ __forceinline__ unsigned lane_route_mask(const int8_t* p, int valid) {
+  if constexpr (C == 16) {
+    const uint4 v = __ldg(reinterpret_cast<const uint4*>(p));
+    return nonzero_bytes(v.x) | (nonzero_bytes(v.y) << 4) | (nonzero_bytes(v.z) << 8) | (nonzero_bytes(v.w) << 12);
+  } else if constexpr (C == 8) {
+    const uint2 v = __ldg(reinterpret_cast<const uint2*>(p));
+    return nonzero_bytes(v.x) | (nonzero_bytes(v.y) << 4);
+  } else if constexpr (C == 4) {
+    return nonzero_bytes(__ldg(reinterpret_cast<const uint32_t*>(p)));
+  } else if constexpr (C == 2) {
+    const uint32_t v = __ldg(reinterpret_cast<const uint16_t*>(p));
+    return nonzero_bytes(v) & 0x3u;
+  } else {
+    unsigned m = 0;
+    for (int b = 0; b < valid; ++b) m |= (__ldg(p + b) != 0 ? 1u : 0u) << b;
+    return m;
+  }
+}
+
+// One warp per token row. Lane l owns the C consecutive experts
+// [base + l*C, base + (l+1)*C) of a 32*C-expert window; an exclusive warp
+// prefix of the per-lane route counts gives every route its output slot, so
+// routes are emitted in increasing expert order. Windows repeat until the
+// row ends or topk routes are out; lanes then fill the remaining slots with
+// -1 / 0.0f.
+template <int C>
 __global__ void __launch_bounds__(kThreads)
     compaction_fwd_kernel(const float* __restrict__ probs, const int8_t* __restrict__ rmap, int64_t T, int32_t E,
                           int32_t topk, float* __restrict__ probs_indices, int32_t* __restrict__ indices) {
-  for (int64_t t = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; t < T; t += (int64_t)gridDim.x * blockDim.x) {
+  const int lane = lane_id();
+  const int64_t warps = (int64_t)gridDim.x * (blockDim.x / kWarp);
+  for (int64_t t = (int64_t)blockIdx.x * (blockDim.x / kWarp) + threadIdx.x / kWarp; t < T; t += warps) {
     const int8_t* row = rmap + t * E;
     const float* prow = probs + t * E;
     float* po = probs_indices + t * topk;
     int32_t* io = indices + t * topk;
-    int j = 0;
-    if (VEC16) {
-      for (int c = 0; c < E && j < topk; c += 16) {
-        const uint4 v = __ldg(reinterpret_cast<const uint4*>(row + c));
-        unsigned mask = nonzero_bytes(v.x) | (nonzero_bytes(v.y) << 4) | (nonzero_bytes(v.z) << 8) |
-                        (nonzero_bytes(v.w) << 12);
-        while (mask != 0u && j < topk) {
-          const int e = c + __ffs(mask) - 1;
-          mask &= mask - 1u;
-          io[j] = e;
-          po[j] = __ldg(prow + e);
-          ++j;
-        }
+    int emitted = 0;
+    for (int base = 0; base < E && emitted < topk; base += kWarp * C) {
+      const int first = base + lane * C;
+      const int valid = min(C, E - first);
+      unsigned mask = valid > 0 ? lane_route_mask<C>(row + first, valid) : 0u;
+      const int cnt = __popc(mask);
+      int excl = cnt;
+#pragma unroll
+      for (int d = 1; d < kWarp; d <<= 1) {
+        const int v = __shfl_up_sync(0xffffffffu, excl, d);
+        if (lane >= d) excl += v;
       }
-    } else {
-      for (int e = 0; e < E && j < topk; ++e) {
-        if (__ldg(row + e) != 0) {
-          io[j] = e;
-          po[j] = __ldg(prow + e);
-          ++j;
-        }
+      const int total = __shfl_sync(0xffffffffu, excl, kWarp - 1);
+      int j = emitted + excl - cnt;
+      while (mask != 0u && j < topk) {
+        const int e = first + __ffs(mask) - 1;
+        mask &= mask - 1u;
+        io[j] = e;
+        po[j] = __ldg(prow + e);
+        ++j;
       }
+      emitted += total;
     }
-    for (; j < topk; ++j) {
+    for (int j = emitted + lane; j < topk; j += kWarp) {
       io[j] = -1;
       po[j] = 0.0f;
     }
@@ -116,12 +148,47 @@ extern "C" int moe_routing_map_to_indices_fwd(const float* probs, const int8_t* 
   if (!aligned(probs, 4) || !aligned(probs_indices, 4) || !aligned(indices, 4)) return MOE_ERR_UNSUPPORTED;
   if (T == 0) return MOE_OK;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  if (E % 16 == 0 && aligned(routing_map, 16)) {
-    auto k = compaction_fwd_kernel<true>;
-    k<<<grid_for(k, T), kThreads, 0, s>>>(probs, routing_map, T, E, topk, probs_indices, indices);
-  } else {
-    auto k = compaction_fwd_kernel<false>;
-    k<<<grid_for(k, T), kThreads, 0, s>>>(probs, routing_map, T, E, topk, probs_indices, indices);
+  // Bytes per lane: the widest C in {16, 8, 4, 2} that divides E, keeps every
+  // map row aligned to C and leaves at most half of the warp idle; else one
+  // byte at a time.
+  int C = 1;
+  for (int c = 16; c >= 2; c >>= 1) {
+    if (E % c == 0 && aligned(routing_map, c) && E >= kWarp * c / 2) {
+      C = c;
+      break;
+    }
+  }
+  const int64_t work_ctas = (T + (kThreads / kWarp) - 1) / (kThreads / kWarp);
+  switch (C) {
+    case 16: {
+      auto k = compaction_fwd_kernel<16>;
+      k<<<persistent_grid(k, kThreads, 0, work_ctas), kThreads, 0, s>>>(probs, routing_map, T, E, topk,
+                                                                          probs_indices, indices);
+      break;
+    }
+    case 8: {
+      auto k = compaction_fwd_kernel<8>;
+      k<<<persistent_grid(k, kThreads, 0, work_ctas), kThreads, 0, s>>>(probs, routing_map, T, E, topk,
+                                                                          probs_indices, indices);
+      break;
+    }
+    case 4: {
+      auto k = compaction_fwd_kernel<4>;
+      k<<<persistent_grid(k, kThreads, 0, work_ctas), kThreads, 0, s>>>(probs, routing_map, T, E, topk,
+                                                                          probs_indices, indices);
+      break;
+    }
+    case 2: {
+      auto k = compaction_fwd_kernel<2>;
+      k<<<persistent_grid(k, kThreads, 0, work_ctas), kThreads, 0, s>>>(probs, routing_map, T, E, topk,
+                                                                          probs_indices, indices);
+      break;
+    }
+    default: {
+      auto k = compaction_fwd_kernel<1>;
+      k<<<persistent_grid(k, kThreads, 0, work_ctas), kThreads, 0, s>>>(probs, routing_map, T, E, topk,
+                                                                          probs_indices, indices);
+    }
   }
   return check_launch();
 }

@@ -192,8 +192,6 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) scatter_kernel(ScatterAr
   using L = Lanes<VB, ET>;
   using V = typename L::V;
   constexpr int NE = L::kElems;
-  constexpr bool kPacked = (NE % 2) == 0;
-  constexpr int NP = kPacked ? NE / 2 : 1;
   constexpr int KR = kKeptInFlight;
   constexpr int KG = kRareGroup;
   const int lane = lane_id();

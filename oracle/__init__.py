@@ -60,6 +60,8 @@ _SIGS = {
     "oracle_routing_map_to_indices_fwd": [_VP, _VP, _I64, _I32, _I32, _VP, _VP],
     "oracle_routing_map_to_indices_bwd": [_VP, _VP, _I64, _I32, _I32, _VP],
     "oracle_f32_to_bf16": [_VP, _I64, _VP],
+    "oracle_binned_gather_weighted": [_VP, _INT, _VP, _VP, _VP, _VP, _I64, _I64, _I32, _I32, _I32, _VP],
+    "oracle_padded_gather_weighted": [_VP, _INT, _VP, _VP, _VP, _VP, _VP, _I64, _I64, _I32, _I32, _VP, _I64],
 }
 
 
@@ -136,6 +138,34 @@ def padded_gather(x, indices, bin_ids, bins, padded_bins, top_k, out_rows=None, 
     rc = lib.oracle_padded_gather(_p(x), _dtype_code(x), _p(_i32(indices)), _p(_i32(bin_ids)),
                                   _p(_i32(bins)), _p(pb), T, H, E, top_k, _p(out), rows)
     _check(rc, "padded_gather")
+    return out
+
+
+def binned_gather_weighted(dy, indices, bin_ids, bins, weights, E, capacity, top_k, lib=None):
+    """Gradient of the binned combine with respect to the expert rows."""
+    lib = lib or load()
+    dy = np.ascontiguousarray(dy)
+    T, H = dy.shape
+    w = None if weights is None else np.ascontiguousarray(weights, dtype=np.float32).reshape(-1)
+    out = np.empty((E, capacity, H), dy.dtype)
+    rc = lib.oracle_binned_gather_weighted(_p(dy), _dtype_code(dy), _p(_i32(indices)), _p(_i32(bin_ids)),
+                                           _p(_i32(bins)), _p(w), T, H, E, capacity, top_k, _p(out))
+    _check(rc, "binned_gather_weighted")
+    return out
+
+
+def padded_gather_weighted(dy, indices, bin_ids, bins, padded_bins, weights, top_k, out_rows=None, lib=None):
+    """Gradient of the padded combine with respect to the expert rows."""
+    lib = lib or load()
+    dy = np.ascontiguousarray(dy)
+    T, H = dy.shape
+    pb = _i32(padded_bins)
+    rows = int(pb[-1]) if out_rows is None else int(out_rows)
+    w = None if weights is None else np.ascontiguousarray(weights, dtype=np.float32).reshape(-1)
+    out = np.empty((rows, H), dy.dtype)
+    rc = lib.oracle_padded_gather_weighted(_p(dy), _dtype_code(dy), _p(_i32(indices)), _p(_i32(bin_ids)),
+                                           _p(_i32(bins)), _p(pb), _p(w), T, H, pb.size, top_k, _p(out), rows)
+    _check(rc, "padded_gather_weighted")
     return out
 
 

@@ -190,6 +190,53 @@ static int gather(const void* x, int dtype, const int32_t* indices, const int32_
     return 0;
 }
 
+/*
+ * Weighted gather: the gradient of the combine with respect to the expert
+ * rows. The pages give the combine ([binned] Workflow step 5; [padded]
+ * Workflow step 6: y[t] = sum over kept slots of weights[a] * row(a)); its
+ * derivative with respect to row(a) is weights[a] * dy[a / TOP_K]. So out
+ * is zero-filled and every kept sorted position i writes
+ * fl(weights[indices[i]] * dy[indices[i] / TOP_K]) to its expert row,
+ * rounded to dtype. weights == NULL gives the plain gather.
+ */
+static int gather_weighted(const void* dy, int dtype, const int32_t* indices, const int32_t* bin_ids,
+                           const int32_t* bins, const int32_t* padded_bins, const float* weights,
+                           int64_t T, int64_t H, int32_t E, int32_t capacity, int32_t top_k, void* out,
+                           int64_t out_rows) {
+    int64_t n = T * top_k;
+    int rc = check_bins(indices, bin_ids, bins, padded_bins, n, E);
+    if (rc) return rc;
+    memset(out, 0, (size_t)out_rows * (size_t)H * elem_size(dtype));
+    for (int64_t i = 0; i < n; ++i) {
+        int64_t row = expert_row(i, bin_ids, bins, padded_bins, capacity);
+        if (row < 0) continue;
+        if (row >= out_rows) return 6;
+        int64_t a = indices[i];
+        int64_t token = a / top_k;
+        for (int64_t h = 0; h < H; ++h) {
+            float v = load_elem(dy, dtype, token * H + h);
+            float scaled = weights ? weights[a] * v : v;
+            store_elem(out, dtype, row * H + h, scaled);
+        }
+    }
+    return 0;
+}
+
+int oracle_binned_gather_weighted(const void* dy, int dtype, const int32_t* indices, const int32_t* bin_ids,
+                                  const int32_t* bins, const float* weights, int64_t T, int64_t H, int32_t E,
+                                  int32_t capacity, int32_t top_k, void* out) {
+    if (capacity < 0) return 2;
+    return gather_weighted(dy, dtype, indices, bin_ids, bins, NULL, weights, T, H, E, capacity, top_k, out,
+                           (int64_t)E * capacity);
+}
+
+int oracle_padded_gather_weighted(const void* dy, int dtype, const int32_t* indices, const int32_t* bin_ids,
+                                  const int32_t* bins, const int32_t* padded_bins, const float* weights,
+                                  int64_t T, int64_t H, int32_t E, int32_t top_k, void* out, int64_t out_rows) {
+    return gather_weighted(dy, dtype, indices, bin_ids, bins, padded_bins, weights, T, H, E, 0, top_k, out,
+                           out_rows);
+}
+
 int oracle_binned_gather(const void* x, int dtype, const int32_t* indices, const int32_t* bin_ids,
                          const int32_t* bins, int64_t T, int64_t H, int32_t E, int32_t capacity,
                          int32_t top_k, void* out) {

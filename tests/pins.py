@@ -212,6 +212,47 @@ def check_wgrad_derivative(lib):
                 assert abs(wg[a] - d) <= 1e-6 * (1 + abs(d)), (mode, a, wg[a], d)
 
 
+def check_weighted_gather(lib):
+    """The weighted gather is the combine's gradient with respect to the
+    expert rows: with no weights (or unit weights) it is the plain gather,
+    and <scatter_w(xe), G> == <xe, gather_w(G)> exactly on integer data with
+    dyadic weights, for both layouts and both dtypes."""
+    g = _rng(31)
+    for te, E, K in _routings():
+        n = te.size
+        T = n // K
+        H = 4
+        r = oracle.route_build(te, E, 3, lib=lib)
+        w = g.choice(np.array([0.5, 1.0, 2.0, -1.0, 0.25], np.float32), size=n)
+        for dt in ("f32", "bf16"):
+            Gf = _xint(T, H, 41)
+            G = Gf if dt == "f32" else oracle.f32_to_bf16(Gf, lib=lib)
+            for cap in (1, 3):
+                plain = oracle.binned_gather(G, r["indices"], r["bin_ids"], r["bins"], E, cap, K, lib=lib)
+                for ones in (None, np.ones(n, np.float32)):
+                    assert np.array_equal(oracle.binned_gather_weighted(G, r["indices"], r["bin_ids"], r["bins"],
+                                                                        ones, E, cap, K, lib=lib), plain)
+                xe_f = _xint(E * cap, H, 42).reshape(E, cap, H)
+                xe = xe_f if dt == "f32" else oracle.f32_to_bf16(xe_f, lib=lib)
+                y = oracle.binned_scatter(xe, r["indices"], r["bin_ids"], r["bins"], w, T, K, lib=lib)
+                gw = oracle.binned_gather_weighted(G, r["indices"], r["bin_ids"], r["bins"], w, E, cap, K, lib=lib)
+                lhs = np.sum(oracle.to_f32(y).astype(np.float64) * oracle.to_f32(G))
+                rhs = np.sum(oracle.to_f32(xe).astype(np.float64) * oracle.to_f32(gw))
+                assert lhs == rhs
+            P = int(r["padded_bins"][-1])
+            plain = oracle.padded_gather(G, r["indices"], r["bin_ids"], r["bins"], r["padded_bins"], K, lib=lib)
+            assert np.array_equal(oracle.padded_gather_weighted(G, r["indices"], r["bin_ids"], r["bins"],
+                                                                r["padded_bins"], None, K, lib=lib), plain)
+            xe_f = _xint(P, H, 43)
+            xe = xe_f if dt == "f32" else oracle.f32_to_bf16(xe_f, lib=lib)
+            y = oracle.padded_scatter(xe, r["indices"], r["bin_ids"], r["bins"], r["padded_bins"], w, T, K, lib=lib)
+            gw = oracle.padded_gather_weighted(G, r["indices"], r["bin_ids"], r["bins"], r["padded_bins"], w, K,
+                                               lib=lib)
+            lhs = np.sum(oracle.to_f32(y).astype(np.float64) * oracle.to_f32(G))
+            rhs = np.sum(oracle.to_f32(xe).astype(np.float64) * oracle.to_f32(gw))
+            assert lhs == rhs
+
+
 def check_compaction(lib):
     """Increasing expert order, valid count min(k_t, topk), probs gathered
     bitwise, -1 / 0.0 padding; brute force over every map row for E <= 6."""
@@ -269,6 +310,12 @@ def check_bruteforce(lib):
                 wg = oracle.padded_wgrad(xe, grad, r["indices"], r["bin_ids"], r["bins"], r["padded_bins"], K, lib=lib)
                 for a in range(n):
                     assert wg[a] == np.float32(np.dot(xe[rows[a]].astype(np.float64), grad[a // K]))
+                gw = oracle.padded_gather_weighted(grad, r["indices"], r["bin_ids"], r["bins"], r["padded_bins"], w,
+                                                   K, lib=lib)
+                want = np.zeros((P, 2), np.float32)
+                for a in range(n):
+                    want[rows[a]] = w[a] * grad[a // K]
+                assert np.array_equal(gw, want)
             r = oracle.route_build(te, E, 1, lib=lib)
             for cap in range(0, n + 1):
                 rows = _ref_rows(te, E, K, cap=cap)
@@ -291,6 +338,12 @@ def check_bruteforce(lib):
                 for a in range(n):
                     want_w = 0.0 if rows[a] < 0 else np.float32(np.dot(flat[rows[a]].astype(np.float64), grad[a // K]))
                     assert wg[a] == want_w
+                gw = oracle.binned_gather_weighted(grad, r["indices"], r["bin_ids"], r["bins"], w, E, cap, K, lib=lib)
+                want = np.zeros((E * cap, 2), np.float32)
+                for a in range(n):
+                    if rows[a] >= 0:
+                        want[rows[a]] = w[a] * grad[a // K]
+                assert np.array_equal(gw.reshape(-1, 2), want)
 
 
 def check_bf16_rounding(lib):
@@ -363,6 +416,11 @@ def check_golden(lib):
     assert oracle.padded_wgrad(xp, grad, r["indices"], r["bin_ids"], r["bins"], r["padded_bins"], K, lib=lib).tolist() \
         == d["padded_wgrad"]
 
+    assert oracle.binned_gather_weighted(grad, r["indices"], r["bin_ids"], r["bins"], w, E, 1, K, lib=lib).reshape(
+        -1, x.shape[1]).tolist() == d["binned_gather_weighted_cap1"]
+    assert oracle.padded_gather_weighted(grad, r["indices"], r["bin_ids"], r["bins"], r["padded_bins"], w, K,
+                                         lib=lib).tolist() == d["padded_gather_weighted"]
+
     c = read_golden("compaction_worked.txt")
     probs = np.array(c["probs"], np.float32)
     rmap = np.array(c["routing_map"], np.int8)
@@ -379,6 +437,7 @@ ALL_CHECKS = [
     check_gather_rows,
     check_roundtrip_kx,
     check_adjoint,
+    check_weighted_gather,
     check_wgrad_derivative,
     check_compaction,
     check_bruteforce,

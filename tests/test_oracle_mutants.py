@@ -29,7 +29,10 @@ MUTANTS = [
     ("binned_row_transposed", "return (int64_t)e * capacity + offset;", "return (int64_t)offset * capacity + e;"),
     ("gather_token_mod", "int64_t token = indices[i] / top_k;\n        memcpy",
      "int64_t token = indices[i] % top_k;\n        memcpy"),
-    ("gather_no_zero", "memset(out, 0, (size_t)out_rows", "memset(out, 1, (size_t)out_rows"),
+    ("gather_no_zero", "memset(out, 0, (size_t)out_rows * (size_t)H * b);",
+     "memset(out, 1, (size_t)out_rows * (size_t)H * b);"),
+    ("wgather_no_zero", "memset(out, 0, (size_t)out_rows * (size_t)H * elem_size(dtype));",
+     "memset(out, 1, (size_t)out_rows * (size_t)H * elem_size(dtype));"),
     ("scatter_weight_index", "float scaled = weights[a] * v;", "float scaled = weights[(a + 1) % n] * v;"),
     ("scatter_drop_term", "acc[h] = acc[h] + scaled;", "acc[h] = scaled;"),
     ("scatter_unweighted_drop_term", "acc[h] = acc[h] + v;", "acc[h] = v;"),
@@ -50,6 +53,11 @@ MUTANTS = [
     ("compaction_bwd_slot_swap", "grad_probs[t * E + e] = grad_probs_indices[t * topk + j];",
      "grad_probs[t * E + e] = grad_probs_indices[t * topk + (topk - 1 - j)];"),
     ("bf16_round_half_up", "u += 0x7fffu + lsb;", "u += 0x8000u;"),
+    ("wgather_weight_by_position", "float scaled = weights ? weights[a] * v : v;",
+     "float scaled = weights ? weights[i] * v : v;"),
+    ("wgather_unscaled", "float scaled = weights ? weights[a] * v : v;", "float scaled = weights ? v : v;"),
+    ("wgather_token_mod", "int64_t a = indices[i];\n        int64_t token = a / top_k;",
+     "int64_t a = indices[i];\n        int64_t token = a % top_k;"),
 ]
 
 _RUNNER = textwrap.dedent("""

@@ -205,6 +205,26 @@ class Path:
                                                                            out=self.gprobs)),
         ]
 
+    def next_ops(self):
+        """(name, callable, algorithmic bytes) of the rows beyond the routing
+        path that are built: the weighted gathers, i.e. the combine's
+        gradient with respect to the expert rows, with grad as dy."""
+        p, r, rt = self.p, self.r, self.route
+        T, H, E, K, n, b = r.T, r.H, r.E, r.K, self.n, 2
+        w = self.pi.view(-1)
+        if not hasattr(self, "gwb"):
+            self.gwb = self.torch.empty_like(self.xb)
+            self.gwp = self.torch.empty_like(self.xp)
+        return [
+            ("binned_gather_weighted",
+             lambda: p.moe_binned_gather_weighted(self.grad, rt.indices, rt.bins, w, E, r.capacity, K, out=self.gwb),
+             self.kept * H * b + E * r.capacity * H * b + 8 * self.kept + 4 * E),
+            ("padded_gather_weighted",
+             lambda: p.moe_padded_gather_weighted(self.grad, rt.indices, rt.bins, rt.padded_bins, w, K,
+                                                  out_rows=self.P, out=self.gwp),
+             n * H * b + self.P * H * b + 8 * n + 8 * E),
+        ]
+
     def algorithmic_bytes(self) -> dict:
         """Bytes each kernel must move (no reuse credited), per launch."""
         r = self.r
@@ -328,6 +348,7 @@ def run_gpu(args, rank, world, local_rank):
     total_ms = max_over_ranks(float(sum(step_ms)), dist, dev)
 
     e2e = run_e2e(args, path, dev, dist)
+    next_rows = time_next_rows(args, path, flush, stream)
 
     if rank != 0:
         if dist is not None:
@@ -363,6 +384,7 @@ def run_gpu(args, rank, world, local_rank):
                      "unit": "GB/s", "frac": round(ach / peak, 4),
                      "traffic": traffic_from_profiles(dominant, libbuild.source_digest())},
         "e2e": e2e,
+        "next_rows": next_rows,
         "gpu_launches": sum(l for _, l, _ in ops) * args.steps,
         "clocks": clocks.summary(),
         "host_timed_s": round(t_host, 4),
@@ -374,6 +396,35 @@ def run_gpu(args, rank, world, local_rank):
     if dist is not None:
         dist.barrier()
         dist.destroy_process_group()
+
+
+def time_next_rows(args, path, flush, stream):
+    """Each built row beyond the routing path, timed alone (L2 flushed before
+    every launch, CUDA events on the launching stream)."""
+    import torch
+
+    peak, peak_kind = measured_peak()
+    out = {}
+    reps = max(3, min(args.steps, 50))
+    for name, fn, nbytes in path.next_ops():
+        for _ in range(3):
+            flush.zero_()
+            fn()
+        ms = []
+        for _ in range(reps):
+            flush.zero_()
+            a = torch.cuda.Event(enable_timing=True)
+            b = torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            fn()
+            b.record(stream)
+            b.synchronize()
+            ms.append(a.elapsed_time(b))
+        mean = statistics.mean(ms)
+        gbs = nbytes / (mean * 1e-3) / 1e9
+        out[name] = {"ms": round(mean, 5), "algorithmic_bytes": nbytes, "gbs": round(gbs, 1),
+                     "frac_of_%s_peak" % peak_kind: round(gbs / peak, 4)}
+    return out
 
 
 def run_e2e(args, path, dev, dist):

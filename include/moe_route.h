@@ -176,6 +176,32 @@ int moe_padded_gather(const void* x, int32_t dtype, const int32_t* indices,
                       int32_t* d_status, moe_stream_t stream);
 
 /*
+ * Weighted gather: the gradient of the combine (moe_*_scatter with weights)
+ * with respect to the expert rows. The pages define the combine ([binned]
+ * Workflow step 5; [padded] Workflow step 6); its derivative with respect to
+ * the row of a kept assignment a is weights[a] * dy[a / top_k]:
+ *   out[row(a), :] = fl(weights[a] * dy[a / top_k, :])  for kept a,
+ *   0                                                 for every other row,
+ * each product rounded to nearest in fp32, then to dtype (nearest even).
+ * Same layout, arguments and row mapping as the plain gathers, with dy [T, H]
+ * in place of x and weights [n] fp32 (required when T > 0). The gradient of
+ * an unweighted combine is the plain gather of dy.
+ */
+int moe_binned_gather_weighted(const void* dy, int32_t dtype,
+                               const int32_t* indices, const int32_t* bins,
+                               const float* weights, int64_t num_tokens,
+                               int64_t hidden, int32_t num_experts,
+                               int32_t capacity, int32_t top_k, void* out,
+                               int32_t* d_status, moe_stream_t stream);
+int moe_padded_gather_weighted(const void* dy, int32_t dtype,
+                               const int32_t* indices, const int32_t* bins,
+                               const int32_t* padded_bins, const float* weights,
+                               int64_t num_tokens, int64_t hidden,
+                               int32_t num_experts, int32_t top_k, void* out,
+                               int64_t out_rows, int32_t* d_status,
+                               moe_stream_t stream);
+
+/*
  * Scatter / combine ([binned] Workflow step 5, Guardrails; [padded]
  * Workflow step 6, Guardrails). For each token t:
  *   out[t, :] = sum_{k=0..top_k-1, slot kept} s_a * xe[row(a), :],

@@ -6,9 +6,11 @@ from ._lib import MoeError, load  # noqa: F401
 from .ops import (  # noqa: F401
     Route,
     moe_binned_gather,
+    moe_binned_gather_weighted,
     moe_binned_scatter,
     moe_binned_wgrad,
     moe_padded_gather,
+    moe_padded_gather_weighted,
     moe_padded_scatter,
     moe_padded_wgrad,
     moe_route_build,

@@ -33,6 +33,9 @@ SIGNATURES = {
     "moe_route_build_noalloc": (ctypes.c_int, [_P, _I64, _I32, _I32, _P, _P, _P, _P, _P, _P, _P]),
     "moe_binned_gather": (ctypes.c_int, [_P, _I32, _P, _P, _I64, _I64, _I32, _I32, _I32, _P, _P, _P]),
     "moe_padded_gather": (ctypes.c_int, [_P, _I32, _P, _P, _P, _I64, _I64, _I32, _I32, _P, _I64, _P, _P]),
+    "moe_binned_gather_weighted": (ctypes.c_int, [_P, _I32, _P, _P, _P, _I64, _I64, _I32, _I32, _I32, _P, _P, _P]),
+    "moe_padded_gather_weighted": (ctypes.c_int, [_P, _I32, _P, _P, _P, _P, _I64, _I64, _I32, _I32, _P, _I64, _P,
+                                                  _P]),
     "moe_scatter_workspace_size": (_SZ, [_I64]),
     "moe_binned_scatter": (ctypes.c_int, [_P, _I32, _P, _P, _P, _P, _P, _I64, _I64, _I32, _I32, _I32, _P, _P, _SZ,
                                           _P, _P]),

@@ -10,8 +10,13 @@
 // and streams it with VB-byte vectors (256-bit loads and stores when the row
 // and pointers allow), U vectors per lane in flight. The bin
 // vectors are staged in shared memory; a padded row finds its expert by
-// binary search over padded_bins.
+// binary search over padded_bins. The weighted variant (the gradient of the
+// combine with respect to the expert rows, d row(a) = w[a] * dy[a / TOP_K])
+// scales each copied row by its assignment's weight on the way through.
 #include "common.cuh"
+#include "vec_math.cuh"
+
+#include <type_traits>
 
 namespace moe {
 namespace {
@@ -25,6 +30,7 @@ struct GatherArgs {
   const int32_t* indices;
   const int32_t* bins;
   const int32_t* padded_bins;  // nullptr: binned
+  const float* weights;        // weighted gather only: scale of each assignment
   int64_t n;
   int64_t rows_out;
   int64_t vecs;  // vectors per row
@@ -34,9 +40,9 @@ struct GatherArgs {
   int32_t* status;
 };
 
-// Source token of output row `row`, or -1 for a zero row.
+// Assignment id whose token fills output row `row`, or -1 for a zero row.
 template <bool PADDED>
-__device__ __forceinline__ int64_t source_token(const GatherArgs& g, const int32_t* sb, const int32_t* spb,
+__device__ __forceinline__ int64_t source_assignment(const GatherArgs& g, const int32_t* sb, const int32_t* spb,
                                                 int64_t row) {
   int32_t e;
   int64_t j, seg_len = 0;
@@ -73,11 +79,38 @@ __device__ __forceinline__ int64_t source_token(const GatherArgs& g, const int32
     flag_status(g.status, MOE_STATUS_BAD_INDEX);
     return -1;
   }
-  return a / g.top_k;
+  return a;
 }
 
-template <int VB, int U, bool PADDED>
+// v scaled by w element-wise, each product rounded to nearest (fp32) and,
+// for bf16 rows, rounded once more to bf16 (nearest even).
+template <typename ET, typename V>
+__device__ __forceinline__ V scale_vec(const V& v, float w) {
+  if constexpr (sizeof(V) == 2) {
+    const float x = __uint_as_float((uint32_t)v << 16);
+    __nv_bfloat16 b = __float2bfloat16_rn(__fmul_rn(w, x));
+    return *reinterpret_cast<uint16_t*>(&b);
+  } else {
+    V r;
+#pragma unroll
+    for (int q = 0; q < Words<V>::N; ++q) {
+      const uint32_t word = Words<V>::get(v, q);
+      if constexpr (Elem<ET>::kBytes == 4) {
+        Words<V>::set(r, q, __float_as_uint(__fmul_rn(w, __uint_as_float(word))));
+      } else {
+        Words<V>::set(r, q, pack_bf16x2(__fmul_rn(w, __uint_as_float(word << 16)),
+                                        __fmul_rn(w, __uint_as_float(word & 0xffff0000u))));
+      }
+    }
+    return r;
+  }
+}
+
+// ST = void: plain row copy; float / __nv_bfloat16: each row scaled by the
+// weight of its assignment (the weighted gather).
+template <int VB, int U, bool PADDED, typename ST>
 __global__ void __launch_bounds__(kThreads) gather_kernel(GatherArgs g) {
+  constexpr bool kWeighted = !std::is_void<ST>::value;
   using V = typename Vec<VB>::T;
   __shared__ int32_t sbins[kStageMax];
   __shared__ int32_t spbins[PADDED ? kStageMax : 1];
@@ -100,10 +133,12 @@ __global__ void __launch_bounds__(kThreads) gather_kernel(GatherArgs g) {
   V* __restrict__ out = reinterpret_cast<V*>(g.out);
   for (int64_t row = (int64_t)blockIdx.x * (blockDim.x / kWarp) + threadIdx.x / kWarp; row < g.rows_out;
        row += warps) {
-    const int64_t src = source_token<PADDED>(g, sb, spb, row);
+    const int64_t a = source_assignment<PADDED>(g, sb, spb, row);
     V* dst = out + row * g.vecs;
-    if (src >= 0) {
-      const V* s = x + src * g.vecs;
+    if (a >= 0) {
+      const V* s = x + (a / g.top_k) * g.vecs;
+      float w = 1.0f;
+      if constexpr (kWeighted) w = __ldg(g.weights + a);
       for (int64_t c0 = 0; c0 < g.vecs; c0 += kWarp * U) {
         V v[U];
 #pragma unroll
@@ -114,7 +149,11 @@ __global__ void __launch_bounds__(kThreads) gather_kernel(GatherArgs g) {
 #pragma unroll
         for (int u = 0; u < U; ++u) {
           const int64_t c = c0 + u * kWarp + lane;
-          if (c < g.vecs) st_stream(dst + c, v[u]);
+          if constexpr (kWeighted) {
+            if (c < g.vecs) st_stream(dst + c, scale_vec<ST>(v[u], w));
+          } else {
+            if (c < g.vecs) st_stream(dst + c, v[u]);
+          }
         }
       }
     } else {
@@ -124,30 +163,40 @@ __global__ void __launch_bounds__(kThreads) gather_kernel(GatherArgs g) {
   }
 }
 
-template <int VB, bool PADDED>
+template <int VB, bool PADDED, typename ST>
 int launch_gather(const GatherArgs& g, cudaStream_t s) {
   constexpr int U = VB == 32 ? 4 : (VB >= 8 ? 8 : 16);  // 128 bytes per lane in flight
-  auto k = gather_kernel<VB, U, PADDED>;
+  auto k = gather_kernel<VB, U, PADDED, ST>;
   const int64_t work_ctas = (g.rows_out + (kThreads / kWarp) - 1) / (kThreads / kWarp);
   const int grid = persistent_grid(k, kThreads, 0, work_ctas);
   k<<<grid, kThreads, 0, s>>>(g);
   return check_launch();
 }
 
-template <bool PADDED>
-int dispatch_gather(GatherArgs g, int elem, const void* x, void* out, cudaStream_t s) {
+template <bool PADDED, typename ST>
+int dispatch_vec(GatherArgs g, int elem, cudaStream_t s) {
   const int64_t row_bytes = g.vecs * elem;  // g.vecs holds H on entry
-  const void* ptrs[] = {x, out};
+  const void* ptrs[] = {g.x, g.out};
   const int vb = pick_vec_bytes(row_bytes, ptrs, 2, elem, 32);
   if (vb == 0) return MOE_ERR_UNSUPPORTED;
   g.vecs = row_bytes / vb;
   switch (vb) {
-    case 32: return launch_gather<32, PADDED>(g, s);
-    case 16: return launch_gather<16, PADDED>(g, s);
-    case 8: return launch_gather<8, PADDED>(g, s);
-    case 4: return launch_gather<4, PADDED>(g, s);
-    default: return launch_gather<2, PADDED>(g, s);
+    case 32: return launch_gather<32, PADDED, ST>(g, s);
+    case 16: return launch_gather<16, PADDED, ST>(g, s);
+    case 8: return launch_gather<8, PADDED, ST>(g, s);
+    case 4: return launch_gather<4, PADDED, ST>(g, s);
+    default:
+      if constexpr (std::is_same<ST, float>::value) return MOE_ERR_UNSUPPORTED;  // fp32 rows are 4-byte multiples
+      else return launch_gather<2, PADDED, ST>(g, s);
   }
+}
+
+template <bool PADDED>
+int dispatch_gather(GatherArgs g, int32_t dtype, cudaStream_t s) {
+  const int elem = dtype_bytes(dtype);
+  if (g.weights == nullptr) return dispatch_vec<PADDED, void>(g, elem, s);
+  if (dtype == MOE_F32) return dispatch_vec<PADDED, float>(g, elem, s);
+  return dispatch_vec<PADDED, __nv_bfloat16>(g, elem, s);
 }
 
 int gather_checks(const void* x, int32_t dtype, const int32_t* indices, const int32_t* bins, int64_t T, int64_t H,
@@ -177,9 +226,9 @@ extern "C" int moe_binned_gather(const void* x, int32_t dtype, const int32_t* in
   const int64_t rows = (int64_t)E * capacity;
   if (rows == 0 || H == 0) return MOE_OK;
   if (out == nullptr) return MOE_ERR_INVALID_ARG;
-  GatherArgs g{static_cast<const char*>(x), static_cast<char*>(out), indices, bins, nullptr, T * top_k, rows, H,
-               E, capacity, top_k, d_status};
-  return dispatch_gather<false>(g, dtype_bytes(dtype), x, out, reinterpret_cast<cudaStream_t>(stream));
+  GatherArgs g{static_cast<const char*>(x), static_cast<char*>(out), indices, bins, nullptr, nullptr, T * top_k,
+               rows, H, E, capacity, top_k, d_status};
+  return dispatch_gather<false>(g, dtype, reinterpret_cast<cudaStream_t>(stream));
 }
 
 extern "C" int moe_padded_gather(const void* x, int32_t dtype, const int32_t* indices, const int32_t* bins,
@@ -191,7 +240,39 @@ extern "C" int moe_padded_gather(const void* x, int32_t dtype, const int32_t* in
   if (!aligned(padded_bins, 4)) return MOE_ERR_UNSUPPORTED;
   if (out_rows == 0 || H == 0) return MOE_OK;
   if (out == nullptr) return MOE_ERR_INVALID_ARG;
-  GatherArgs g{static_cast<const char*>(x), static_cast<char*>(out), indices, bins, padded_bins, T * top_k, out_rows,
-               H, E, 0, top_k, d_status};
-  return dispatch_gather<true>(g, dtype_bytes(dtype), x, out, reinterpret_cast<cudaStream_t>(stream));
+  GatherArgs g{static_cast<const char*>(x), static_cast<char*>(out), indices, bins, padded_bins, nullptr, T * top_k,
+               out_rows, H, E, 0, top_k, d_status};
+  return dispatch_gather<true>(g, dtype, reinterpret_cast<cudaStream_t>(stream));
+}
+
+extern "C" int moe_binned_gather_weighted(const void* dy, int32_t dtype, const int32_t* indices, const int32_t* bins,
+                                          const float* weights, int64_t T, int64_t H, int32_t E, int32_t capacity,
+                                          int32_t top_k, void* out, int32_t* d_status, moe_stream_t stream) {
+  const int rc = gather_checks(dy, dtype, indices, bins, T, H, E, top_k, out, d_status);
+  if (rc != MOE_OK) return rc;
+  if (capacity < 0) return MOE_ERR_INVALID_ARG;
+  if (weights != nullptr && !aligned(weights, 4)) return MOE_ERR_UNSUPPORTED;
+  if (T > 0 && weights == nullptr) return MOE_ERR_INVALID_ARG;
+  const int64_t rows = (int64_t)E * capacity;
+  if (rows == 0 || H == 0) return MOE_OK;
+  if (out == nullptr) return MOE_ERR_INVALID_ARG;
+  GatherArgs g{static_cast<const char*>(dy), static_cast<char*>(out), indices, bins, nullptr, weights, T * top_k,
+               rows, H, E, capacity, top_k, d_status};
+  return dispatch_gather<false>(g, dtype, reinterpret_cast<cudaStream_t>(stream));
+}
+
+extern "C" int moe_padded_gather_weighted(const void* dy, int32_t dtype, const int32_t* indices, const int32_t* bins,
+                                          const int32_t* padded_bins, const float* weights, int64_t T, int64_t H,
+                                          int32_t E, int32_t top_k, void* out, int64_t out_rows, int32_t* d_status,
+                                          moe_stream_t stream) {
+  const int rc = gather_checks(dy, dtype, indices, bins, T, H, E, top_k, out, d_status);
+  if (rc != MOE_OK) return rc;
+  if (padded_bins == nullptr || out_rows < 0) return MOE_ERR_INVALID_ARG;
+  if (!aligned(padded_bins, 4) || (weights != nullptr && !aligned(weights, 4))) return MOE_ERR_UNSUPPORTED;
+  if (T > 0 && weights == nullptr) return MOE_ERR_INVALID_ARG;
+  if (out_rows == 0 || H == 0) return MOE_OK;
+  if (out == nullptr) return MOE_ERR_INVALID_ARG;
+  GatherArgs g{static_cast<const char*>(dy), static_cast<char*>(out), indices, bins, padded_bins, weights,
+               T * top_k, out_rows, H, E, 0, top_k, d_status};
+  return dispatch_gather<true>(g, dtype, reinterpret_cast<cudaStream_t>(stream));
 }

@@ -116,6 +116,47 @@ def moe_padded_gather(x: torch.Tensor, indices: torch.Tensor, bins: torch.Tensor
     return out
 
 
+def moe_binned_gather_weighted(dy: torch.Tensor, indices: torch.Tensor, bins: torch.Tensor, weights: torch.Tensor,
+                               num_experts: int, capacity: int, top_k: int, out: torch.Tensor | None = None,
+                               status: torch.Tensor | None = None) -> torch.Tensor:
+    """Gradient of the binned combine with respect to the expert rows:
+    dy [T, H] -> [E, capacity, H], row of kept a = weights[a] * dy[a // K]."""
+    _need(dy, None, "dy")
+    dt = _act_dtype(dy, "dy")
+    T, H = dy.shape
+    _need(indices, torch.int32, "indices", dy.device)
+    _need(bins, torch.int32, "bins", dy.device)
+    _need(weights, torch.float32, "weights", dy.device)
+    if out is None:
+        out = torch.empty((num_experts, capacity, H), dtype=dy.dtype, device=dy.device)
+    _need(out, dy.dtype, "out", dy.device)
+    _lib.call("moe_binned_gather_weighted", _ptr(dy), dt, _ptr(indices), _ptr(bins), _ptr(weights), T, H,
+              num_experts, capacity, top_k, _ptr(out), _ptr(status), _stream(dy))
+    return out
+
+
+def moe_padded_gather_weighted(dy: torch.Tensor, indices: torch.Tensor, bins: torch.Tensor,
+                               padded_bins: torch.Tensor, weights: torch.Tensor, top_k: int,
+                               out_rows: int | None = None, out: torch.Tensor | None = None,
+                               status: torch.Tensor | None = None) -> torch.Tensor:
+    """Gradient of the padded combine with respect to the expert rows."""
+    _need(dy, None, "dy")
+    dt = _act_dtype(dy, "dy")
+    T, H = dy.shape
+    _need(indices, torch.int32, "indices", dy.device)
+    _need(bins, torch.int32, "bins", dy.device)
+    _need(padded_bins, torch.int32, "padded_bins", dy.device)
+    _need(weights, torch.float32, "weights", dy.device)
+    if out_rows is None:
+        out_rows = int(padded_bins[-1].item()) if out is None else out.shape[0]
+    if out is None:
+        out = torch.empty((out_rows, H), dtype=dy.dtype, device=dy.device)
+    _need(out, dy.dtype, "out", dy.device)
+    _lib.call("moe_padded_gather_weighted", _ptr(dy), dt, _ptr(indices), _ptr(bins), _ptr(padded_bins),
+              _ptr(weights), T, H, padded_bins.numel(), top_k, _ptr(out), out_rows, _ptr(status), _stream(dy))
+    return out
+
+
 def scatter_workspace(n: int, device) -> torch.Tensor:
     size = _lib.load().moe_scatter_workspace_size(n)
     return torch.empty(max(1, (size + 3) // 4), dtype=torch.int32, device=device)

@@ -18,7 +18,7 @@ def lib():
 
 def test_header_and_exports_agree(lib):
     declared = _lib.header_functions()
-    assert len(declared) == len(set(declared)) == 14
+    assert len(declared) == len(set(declared)) == 16
     out = subprocess.run(["nm", "-D", "--defined-only", _lib.LIB_PATH], capture_output=True, text=True,
                          check=True).stdout
     exported = {ln.split()[-1] for ln in out.splitlines() if " T " in ln}
@@ -73,6 +73,11 @@ def test_host_validation_rejects_bad_arguments(lib):
                                   None) == 1
     assert lib.moe_binned_wgrad(FAKE, None, 0, FAKE, FAKE, FAKE, 4, 8, 2, 4, 1, FAKE, None, None) == 1
     assert lib.moe_padded_wgrad(FAKE, FAKE, 0, FAKE, FAKE, FAKE, FAKE, 4, 8, 2, 1, -3, FAKE, None, None) == 1
+    # weighted gather: weights required when there are tokens; misaligned weights
+    assert lib.moe_binned_gather_weighted(FAKE, 1, FAKE, FAKE, None, 4, 8, 2, 2, 1, FAKE, None, None) == 1
+    assert lib.moe_binned_gather_weighted(FAKE, 1, FAKE, FAKE, FAKE + 2, 4, 8, 2, 2, 1, FAKE, None, None) == 2
+    assert lib.moe_padded_gather_weighted(FAKE, 0, FAKE, FAKE, None, FAKE, 4, 8, 2, 1, FAKE, 8, None, None) == 1
+    assert lib.moe_padded_gather_weighted(FAKE, 0, FAKE, FAKE, FAKE, None, 4, 8, 2, 1, FAKE, 8, None, None) == 1
     assert lib.moe_routing_map_to_indices_fwd(FAKE, FAKE, -1, 4, 2, FAKE, FAKE, None) == 1
     assert lib.moe_routing_map_to_indices_fwd(FAKE, FAKE, 4, 4, 0, FAKE, FAKE, None) == 1
     assert lib.moe_routing_map_to_indices_fwd(FAKE + 1, FAKE, 4, 4, 2, FAKE, FAKE, None) == 2

@@ -1,4 +1,5 @@
-"""GPU parity: every entry point of the CUDA library against the CPU oracle,
+"""GPU parity: every entry point of the CUDA library against the CPU oracle
+(including the weighted gather, the combine's gradient for the expert rows),
 element by element, on the named workloads (tiny fp32, Mixtral-8x7B binned,
 Mixtral-8x22B padded, DeepSeek-V3 binned and padded, Qwen2-MoE-57B
 compaction) at full size and on an edge matrix (empty experts, capacity 0 /
@@ -6,7 +7,8 @@ compaction) at full size and on an edge matrix (empty experts, capacity 0 /
 hidden sizes with ragged tails, T = 0 and 1, misaligned pointers, poisoned
 padding rows, invalid device data reported through the status word).
 
-Gates: bit-exact for route build, gather, compaction and unweighted scatter;
+Gates: bit-exact for route build, gather (plain and weighted), compaction and
+unweighted scatter;
 weighted scatter within 1e-5*(1+|ref|) for fp32 outputs and 2e-2 relative
 for bf16 outputs (and, by construction, bit-exact as well); wgrad within
 1e-5*(1+|ref|) (it is always an fp32 output).
@@ -91,6 +93,9 @@ def run_routing(r: wl.Routing, binned=True, padded=True, poison=True, misalign=F
         wg = p.moe_binned_wgrad(xe, grad, route.indices, route.bin_ids, route.bins, K, status=st)
         o_wg = oracle.binned_wgrad(xe_np, r.grad, o["indices"], o["bin_ids"], o["bins"], K)
         assert_close_fp32(to_host(wg), o_wg, r.name + " binned_wgrad")
+        gw = p.moe_binned_gather_weighted(grad, route.indices, route.bins, w, E, cap, K, status=st)
+        o_gw = oracle.binned_gather_weighted(r.grad, o["indices"], o["bin_ids"], o["bins"], r.weights, E, cap, K)
+        assert_bits_equal(to_host(gw), o_gw, r.name + " binned_gather_weighted")
 
     if padded:
         P = int(o["padded_bins"][-1]) if E else 0
@@ -116,6 +121,11 @@ def run_routing(r: wl.Routing, binned=True, padded=True, poison=True, misalign=F
         wg = p.moe_padded_wgrad(xe, grad, route.indices, route.bin_ids, route.bins, route.padded_bins, K, status=st)
         o_wg = oracle.padded_wgrad(xe_np, r.grad, o["indices"], o["bin_ids"], o["bins"], o["padded_bins"], K)
         assert_close_fp32(to_host(wg), o_wg, r.name + " padded_wgrad")
+        gw = p.moe_padded_gather_weighted(grad, route.indices, route.bins, route.padded_bins, w, K, out_rows=P,
+                                          status=st)
+        o_gw = oracle.padded_gather_weighted(r.grad, o["indices"], o["bin_ids"], o["bins"], o["padded_bins"],
+                                             r.weights, K)
+        assert_bits_equal(to_host(gw), o_gw, r.name + " padded_gather_weighted")
     torch.cuda.synchronize()
     assert int(st.item()) == 0, "device status %d on valid input" % int(st.item())
 

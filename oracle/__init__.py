@@ -37,7 +37,7 @@ def build(force: bool = False, src: str = _SRC, out: str = _LIB) -> str:
     if force or not os.path.exists(out) or os.path.getmtime(out) < os.path.getmtime(src):
         tmp = out + ".tmp%d" % os.getpid()
         subprocess.run(["gcc", "-O2", "-ffp-contract=off", "-fno-fast-math", "-std=c11",
-                        "-shared", "-fPIC", "-o", tmp, src], check=True)
+                        "-shared", "-fPIC", "-o", tmp, src, "-lm"], check=True)
         os.replace(tmp, out)
     return out
 
@@ -60,6 +60,7 @@ _SIGS = {
     "oracle_routing_map_to_indices_fwd": [_VP, _VP, _I64, _I32, _I32, _VP, _VP],
     "oracle_routing_map_to_indices_bwd": [_VP, _VP, _I64, _I32, _I32, _VP],
     "oracle_f32_to_bf16": [_VP, _I64, _VP],
+    "oracle_topk_gating": [_VP, _I64, _I32, _I32, _INT, _INT, _VP, _VP],
     "oracle_binned_gather_weighted": [_VP, _INT, _VP, _VP, _VP, _VP, _I64, _I64, _I32, _I32, _I32, _VP],
     "oracle_padded_gather_weighted": [_VP, _INT, _VP, _VP, _VP, _VP, _VP, _I64, _I64, _I32, _I32, _VP, _I64],
 }
@@ -248,6 +249,20 @@ def routing_map_to_indices_bwd(grad_probs_indices, indices, E, lib=None, allow_b
     if not allow_bad:
         _check(rc, "routing_map_to_indices_bwd")
     return out
+
+
+def topk_gating(logits, top_k, mode="softmax", normalize=True, lib=None):
+    """(top_expert int32 [T, top_k], weights float32 [T, top_k]) from router
+    logits [T, E]; mode "softmax" or "sigmoid"."""
+    lib = lib or load()
+    lg = np.ascontiguousarray(logits, dtype=np.float32)
+    T, E = lg.shape
+    te = np.empty((T, top_k), np.int32)
+    w = np.empty((T, top_k), np.float32)
+    rc = lib.oracle_topk_gating(_p(lg), T, E, top_k, {"softmax": 0, "sigmoid": 1}[mode], int(bool(normalize)),
+                                _p(te), _p(w))
+    _check(rc, "topk_gating")
+    return te, w
 
 
 def f32_to_bf16(a, lib=None):

@@ -43,6 +43,7 @@
  * break the invariants it relies on (it then leaves outputs unspecified but
  * never reads or writes out of bounds).
  */
+#include <math.h>
 #include <stdint.h>
 #include <stdlib.h>
 #include <string.h>
@@ -410,6 +411,73 @@ int oracle_routing_map_to_indices_bwd(const float* grad_probs_indices, const int
         }
     }
     return rc;
+}
+
+/*
+ * Router top-k gating ("Fused MoE Dispatch (Triton, universal)": the
+ * pipeline "router scores -> top-k gating -> permute", usage example with
+ * gating="softmax" or "sigmoid"). Per token t:
+ *   - the top_k experts with the largest logits, in decreasing logit order,
+ *     ties to the lower expert id (a NaN logit counts as -infinity); both
+ *     scores below increase with the logit, so this is the top_k by score;
+ *   - score of expert e: softmax over all E logits (mode 0) or the logistic
+ *     sigmoid of its logit (mode 1), in double;
+ *   - weights[t][k] = score of the k-th chosen expert, divided by the sum of
+ *     the chosen scores when normalize != 0; rounded to fp32 once.
+ * Degenerate rows (every logit -inf or NaN, or chosen scores summing to 0)
+ * take the limit of equal logits: a uniform softmax, weights 1 / top_k.
+ * Requires 1 <= top_k <= E.
+ */
+int oracle_topk_gating(const float* logits, int64_t T, int32_t E, int32_t top_k, int mode, int normalize,
+                       int32_t* top_expert, float* weights) {
+    if (T < 0 || E < 1 || top_k < 1 || top_k > E || (mode != 0 && mode != 1)) return 2;
+    char* chosen = (char*)malloc((size_t)E);
+    double* score = (double*)malloc((size_t)E * sizeof(double));
+    if (!chosen || !score) { free(chosen); free(score); return 7; }
+    for (int64_t t = 0; t < T; ++t) {
+        const float* l = logits + t * E;
+        double lmax = -INFINITY;
+        for (int32_t e = 0; e < E; ++e) {
+            double v = isnan(l[e]) ? -INFINITY : (double)l[e];
+            if (v > lmax) lmax = v;
+        }
+        double z = 0.0;
+        for (int32_t e = 0; e < E; ++e) {
+            double v = isnan(l[e]) ? -INFINITY : (double)l[e];
+            if (mode == 0) {
+                /* every logit -inf: the limit of equal logits, a uniform softmax */
+                score[e] = lmax == -INFINITY ? 1.0 : exp(v - lmax);
+                z += score[e];
+            } else {
+                score[e] = 1.0 / (1.0 + exp(-v));
+            }
+        }
+        if (mode == 0)
+            for (int32_t e = 0; e < E; ++e) score[e] /= z;
+        memset(chosen, 0, (size_t)E);
+        double chosen_sum = 0.0;
+        for (int32_t k = 0; k < top_k; ++k) {
+            int32_t best = -1;
+            float bv = 0.0f;
+            for (int32_t e = 0; e < E; ++e) {
+                if (chosen[e]) continue;
+                float v = isnan(l[e]) ? -INFINITY : l[e];
+                if (best < 0 || v > bv) { best = e; bv = v; }
+            }
+            chosen[best] = 1;
+            top_expert[t * top_k + k] = best;
+            chosen_sum += score[best];
+        }
+        for (int32_t k = 0; k < top_k; ++k) {
+            double w = score[top_expert[t * top_k + k]];
+            /* chosen scores all zero: the limit of equal scores, 1 / top_k each */
+            if (normalize) w = chosen_sum > 0.0 ? w / chosen_sum : 1.0 / top_k;
+            weights[t * top_k + k] = (float)w;
+        }
+    }
+    free(chosen);
+    free(score);
+    return 0;
 }
 
 /* Round fp32 values to bf16 bits (test helper for expected outputs). */

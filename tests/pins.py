@@ -253,6 +253,96 @@ def check_weighted_gather(lib):
             assert lhs == rhs
 
 
+def _gating_logits(seed):
+    g = _rng(seed)
+    cases = []
+    for T, E in [(40, 8), (33, 64), (17, 256), (9, 3)]:
+        lg = g.standard_normal((T, E)).astype(np.float32)
+        lg[::4, : E // 2] = np.round(lg[::4, : E // 2])  # rows with ties
+        cases.append(lg)
+    lg = g.standard_normal((6, 16)).astype(np.float32)
+    lg[0, 3] = np.nan
+    lg[1, :] = -np.inf
+    lg[2, :] = 0.0
+    cases.append(lg)
+    return cases
+
+
+def check_gating_golden(lib):
+    """Hand-worked gating rows (tests/golden/gating_worked.txt)."""
+    d = read_golden("gating_worked.txt")
+    te, w = oracle.topk_gating(np.array(d["softmax_logits"], np.float32), 2, "softmax", True, lib=lib)
+    assert te.tolist() == d["softmax_top_expert"]
+    assert np.allclose(w, d["softmax_weights"], rtol=0, atol=1e-7)
+    lg = np.array(d["sigmoid_logits"], np.float32)
+    te, w = oracle.topk_gating(lg, 2, "sigmoid", True, lib=lib)
+    assert te.tolist() == d["sigmoid_top_expert"] and np.allclose(w, d["sigmoid_weights_normalized"], atol=1e-7)
+    te, w = oracle.topk_gating(lg, 2, "sigmoid", False, lib=lib)
+    assert te.tolist() == d["sigmoid_top_expert"] and np.allclose(w, d["sigmoid_weights_raw"], atol=1e-7)
+
+
+def check_gating_textbook(lib):
+    """The chosen experts are the first top_k of numpy's lexsort by
+    (-logit, expert id) (NaN as -inf); weights equal torch's softmax /
+    sigmoid in double, renormalised over the chosen when asked."""
+    import torch
+
+    for lg in _gating_logits(7):
+        T, E = lg.shape
+        key = np.where(np.isnan(lg), -np.inf, lg).astype(np.float64)
+        for k in sorted({1, 2, min(E, 8), E}):
+            for mode in ("softmax", "sigmoid"):
+                for norm in (True, False):
+                    te, w = oracle.topk_gating(lg, k, mode, norm, lib=lib)
+                    ref_s = (torch.softmax(torch.from_numpy(key), dim=1) if mode == "softmax"
+                             else torch.sigmoid(torch.from_numpy(key))).numpy()
+                    for t in range(T):
+                        order = np.lexsort((np.arange(E), -key[t]))[:k]
+                        assert te[t].tolist() == order.tolist()
+                        want = ref_s[t, order]
+                        if np.all(key[t] == -np.inf):  # degenerate row: limit of equal logits
+                            want = np.full(k, 1.0 / E if mode == "softmax" else 0.0)
+                        if norm:
+                            want = want / want.sum() if want.sum() > 0 else np.full(k, 1.0 / k)
+                        assert np.allclose(w[t], want, rtol=2e-7, atol=1e-12), (mode, norm, t)
+
+
+def check_gating_invariants(lib):
+    """Closed forms: chosen experts distinct, logits non-increasing along the
+    slots with ties in increasing id, no unchosen expert above the last
+    chosen one; normalised weights sum to one; softmax with k = E sums to one
+    unnormalised; softmax weight ratios equal exp(logit differences); a raw
+    sigmoid weight w inverts to its logit, log(w / (1 - w))."""
+    for lg in _gating_logits(11):
+        T, E = lg.shape
+        key = np.where(np.isnan(lg), -np.inf, lg).astype(np.float64)
+        for k in sorted({1, 2, min(E, 8), E}):
+            te, wn = oracle.topk_gating(lg, k, "softmax", True, lib=lib)
+            _, ws = oracle.topk_gating(lg, k, "softmax", False, lib=lib)
+            _, wg = oracle.topk_gating(lg, k, "sigmoid", False, lib=lib)
+            for t in range(T):
+                ex = te[t].tolist()
+                assert len(set(ex)) == k and all(0 <= e < E for e in ex)
+                for j in range(k - 1):
+                    a, b = key[t, ex[j]], key[t, ex[j + 1]]
+                    assert a > b or (a == b and ex[j] < ex[j + 1])
+                rest = [e for e in range(E) if e not in ex]
+                if rest:
+                    last = key[t, ex[-1]]
+                    assert all(key[t, e] < last or (key[t, e] == last and e > ex[-1]) for e in rest)
+                assert abs(float(wn[t].astype(np.float64).sum()) - 1.0) < 1e-6
+                if k == E:
+                    assert abs(float(ws[t].astype(np.float64).sum()) - 1.0) < 1e-6
+                if np.isfinite(key[t, ex]).all():
+                    for j in range(1, k):
+                        if ws[t, j] > 1e-30:
+                            assert abs(np.log(ws[t, 0] / ws[t, j]) - (key[t, ex[0]] - key[t, ex[j]])) < 1e-5
+                    for j in range(k):
+                        w = float(wg[t, j])
+                        if 1e-6 < w < 1 - 1e-6:
+                            assert abs(np.log(w / (1 - w)) - key[t, ex[j]]) < 1e-4 * (1 + abs(key[t, ex[j]]))
+
+
 def check_compaction(lib):
     """Increasing expert order, valid count min(k_t, topk), probs gathered
     bitwise, -1 / 0.0 padding; brute force over every map row for E <= 6."""
@@ -440,6 +530,9 @@ ALL_CHECKS = [
     check_weighted_gather,
     check_wgrad_derivative,
     check_compaction,
+    check_gating_golden,
+    check_gating_textbook,
+    check_gating_invariants,
     check_bruteforce,
     check_bf16_rounding,
     check_bf16_golden,

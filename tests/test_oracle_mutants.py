@@ -53,6 +53,14 @@ MUTANTS = [
     ("compaction_bwd_slot_swap", "grad_probs[t * E + e] = grad_probs_indices[t * topk + j];",
      "grad_probs[t * E + e] = grad_probs_indices[t * topk + (topk - 1 - j)];"),
     ("bf16_round_half_up", "u += 0x7fffu + lsb;", "u += 0x8000u;"),
+    ("gating_ties_to_higher_id", "if (best < 0 || v > bv) { best = e; bv = v; }",
+     "if (best < 0 || v >= bv) { best = e; bv = v; }"),
+    ("gating_sigmoid_sign", "score[e] = 1.0 / (1.0 + exp(-v));", "score[e] = 1.0 / (1.0 + exp(v));"),
+    ("gating_no_normalize", "if (normalize) w = chosen_sum > 0.0 ? w / chosen_sum : 1.0 / top_k;",
+     "if (normalize) w = chosen_sum > 0.0 ? w : 1.0 / top_k;"),
+    ("gating_weight_of_slot", "double w = score[top_expert[t * top_k + k]];", "double w = score[k];"),
+    ("gating_softmax_unscaled", "for (int32_t e = 0; e < E; ++e) score[e] /= z;",
+     "for (int32_t e = 0; e < E; ++e) score[e] /= 1.0;"),
     ("wgather_weight_by_position", "float scaled = weights ? weights[a] * v : v;",
      "float scaled = weights ? weights[i] * v : v;"),
     ("wgather_unscaled", "float scaled = weights ? weights[a] * v : v;", "float scaled = weights ? v : v;"),

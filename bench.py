@@ -207,7 +207,8 @@ class Path:
 
     def next_ops(self):
         """(name, callable, algorithmic bytes) of the rows beyond the routing
-        path that are built: the weighted gathers, i.e. the combine's
+        path that are built: router top-k gating (sigmoid, renormalised, on
+        N(0,1) logits [T, E]) and the weighted gathers, i.e. the combine's
         gradient with respect to the expert rows, with grad as dy."""
         p, r, rt = self.p, self.r, self.route
         T, H, E, K, n, b = r.T, r.H, r.E, r.K, self.n, 2
@@ -215,7 +216,12 @@ class Path:
         if not hasattr(self, "gwb"):
             self.gwb = self.torch.empty_like(self.xb)
             self.gwp = self.torch.empty_like(self.xp)
+            self.logits = self.torch.from_numpy(wl.normal((T, E), wl.F32, r.seed, 11)).to(self.dev)
+            self.g_out = (self.torch.empty((T, K), dtype=self.torch.int32, device=self.dev),
+                          self.torch.empty((T, K), dtype=self.torch.float32, device=self.dev))
         return [
+            ("topk_gating", lambda: p.moe_topk_gating(self.logits, K, "sigmoid", True, out=self.g_out),
+             T * E * 4 + T * K * 8),
             ("binned_gather_weighted",
              lambda: p.moe_binned_gather_weighted(self.grad, rt.indices, rt.bins, w, E, r.capacity, K, out=self.gwb),
              self.kept * H * b + E * r.capacity * H * b + 8 * self.kept + 4 * E),

@@ -4,8 +4,9 @@
  *
  * The library implements the data-parallel routing path of a
  * MegaBlocks-style Mixture-of-Experts layer:
- *   route build -> binned / padded gather (permute) -> [expert FFN, not here]
- *   -> binned / padded scatter (combine) -> router-weight gradient,
+ *   [top-k gating] -> route build -> binned / padded gather (permute)
+ *   -> [expert FFN, not here] -> binned / padded scatter (combine)
+ *   -> router-weight gradient and expert-row gradient (weighted gather),
  * plus the dense routing-map -> fixed-width top-k compaction and its
  * backward. Sources, by page title and section:
  *   [binned] "Build Triton-Ascend Binned MoE Routing": Goal, Workflow,
@@ -14,6 +15,7 @@
  *            Implementation Pattern, Ascend Guardrails, Verification.
  *   [mok]    Megatron-Core API docs, core.transformer.moe.megakernel.mok.
  *            route_adapter: RoutingMapToIndices, routing_map_to_mok_inputs.
+ *   [dispatch] "Fused MoE Dispatch (Triton, universal)": pipeline and usage.
  *
  * Conventions (all entry points):
  *  - Every pointer is a DEVICE pointer owned by the caller. The library
@@ -256,6 +258,32 @@ int moe_padded_wgrad(const void* xe, const void* grad, int32_t dtype,
                      int64_t num_tokens, int64_t hidden, int32_t num_experts,
                      int32_t top_k, int64_t xe_rows, float* wgrad,
                      int32_t* d_status, moe_stream_t stream);
+
+/*
+ * Router top-k gating: the step before the route build ("Fused MoE Dispatch
+ * (Triton, universal)": pipeline "router scores -> top-k gating -> permute",
+ * usage gating="softmax" | "sigmoid"). For each token t:
+ *   top_expert[t, 0..top_k) = the top_k experts by logit, decreasing, ties to
+ *                             the lower expert id (NaN counts as -inf);
+ *   weights[t, k]           = score of expert top_expert[t, k]:
+ *       MOE_GATING_SOFTMAX: softmax over all E logits of the row,
+ *       MOE_GATING_SIGMOID: 1 / (1 + exp(-logit)),
+ *     divided by the sum of the chosen scores when normalize != 0.
+ * Rows with every logit -inf (or chosen scores summing to 0) take the limit
+ * of equal logits: a uniform softmax and weights 1 / top_k. Scores are
+ * computed in fp32 (the selection is an exact comparison of the fp32
+ * logits). top_expert is the route build's input (n = T * top_k) and weights
+ * the combine's.
+ *   logits [T, E] fp32; top_expert [T, top_k] int32 out; weights [T, top_k]
+ *   fp32 out. 1 <= top_k <= min(E, MOE_MAX_TOP_K); E <= MOE_GATING_MAX_EXPERTS
+ *   (else MOE_ERR_UNSUPPORTED).
+ */
+enum moe_gating { MOE_GATING_SOFTMAX = 0, MOE_GATING_SIGMOID = 1 };
+#define MOE_GATING_MAX_EXPERTS 1024
+int moe_topk_gating(const float* logits, int64_t num_tokens,
+                    int32_t num_experts, int32_t top_k, int32_t mode,
+                    int32_t normalize, int32_t* top_expert, float* weights,
+                    moe_stream_t stream);
 
 /*
  * Dense routing map -> fixed-width compaction ([mok] RoutingMapToIndices,

@@ -16,4 +16,5 @@ from .ops import (  # noqa: F401
     moe_route_build,
     moe_routing_map_to_indices_bwd,
     moe_routing_map_to_indices_fwd,
+    moe_topk_gating,
 )

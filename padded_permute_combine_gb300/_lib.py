@@ -18,6 +18,8 @@ MOE_OK, MOE_ERR_INVALID_ARG, MOE_ERR_UNSUPPORTED, MOE_ERR_CUDA = 0, 1, 2, 3
 MOE_F32, MOE_BF16 = 0, 1
 MOE_STATUS_BAD_EXPERT, MOE_STATUS_BAD_INDEX, MOE_STATUS_BAD_BINS, MOE_STATUS_ROWS_MISMATCH = 1, 2, 4, 8
 MOE_MAX_EXPERTS, MOE_MAX_TOP_K = 4096, 64
+MOE_GATING_SOFTMAX, MOE_GATING_SIGMOID = 0, 1
+MOE_GATING_MAX_EXPERTS = 1024
 
 _P = ctypes.c_void_p
 _I64 = ctypes.c_int64
@@ -43,6 +45,7 @@ SIGNATURES = {
                                           _SZ, _P, _P]),
     "moe_binned_wgrad": (ctypes.c_int, [_P, _P, _I32, _P, _P, _P, _I64, _I64, _I32, _I32, _I32, _P, _P, _P]),
     "moe_padded_wgrad": (ctypes.c_int, [_P, _P, _I32, _P, _P, _P, _P, _I64, _I64, _I32, _I32, _I64, _P, _P, _P]),
+    "moe_topk_gating": (ctypes.c_int, [_P, _I64, _I32, _I32, _I32, _I32, _P, _P, _P]),
     "moe_routing_map_to_indices_fwd": (ctypes.c_int, [_P, _P, _I64, _I32, _I32, _P, _P, _P]),
     "moe_routing_map_to_indices_bwd": (ctypes.c_int, [_P, _P, _I64, _I32, _I32, _P, _P, _P]),
 }

@@ -252,6 +252,21 @@ def moe_padded_wgrad(xe: torch.Tensor, grad: torch.Tensor, indices: torch.Tensor
     return out
 
 
+def moe_topk_gating(logits: torch.Tensor, top_k: int, mode: str = "softmax", normalize: bool = True,
+                    out: tuple[torch.Tensor, torch.Tensor] | None = None):
+    """(top_expert int32 [T, top_k], weights fp32 [T, top_k]) from router
+    logits [T, E]; mode "softmax" or "sigmoid"."""
+    _need(logits, torch.float32, "logits")
+    T, E = logits.shape
+    m = {"softmax": _lib.MOE_GATING_SOFTMAX, "sigmoid": _lib.MOE_GATING_SIGMOID}[mode]
+    if out is None:
+        out = (torch.empty((T, top_k), dtype=torch.int32, device=logits.device),
+               torch.empty((T, top_k), dtype=torch.float32, device=logits.device))
+    _lib.call("moe_topk_gating", _ptr(logits), T, E, top_k, m, int(bool(normalize)), _ptr(out[0]), _ptr(out[1]),
+              _stream(logits))
+    return out
+
+
 def moe_routing_map_to_indices_fwd(probs: torch.Tensor, routing_map: torch.Tensor, topk: int,
                                    out: tuple[torch.Tensor, torch.Tensor] | None = None):
     """(probs_indices [T, topk] fp32, indices [T, topk] int32) from a dense

@@ -18,7 +18,7 @@ def lib():
 
 def test_header_and_exports_agree(lib):
     declared = _lib.header_functions()
-    assert len(declared) == len(set(declared)) == 16
+    assert len(declared) == len(set(declared)) == 17
     out = subprocess.run(["nm", "-D", "--defined-only", _lib.LIB_PATH], capture_output=True, text=True,
                          check=True).stdout
     exported = {ln.split()[-1] for ln in out.splitlines() if " T " in ln}
@@ -78,6 +78,11 @@ def test_host_validation_rejects_bad_arguments(lib):
     assert lib.moe_binned_gather_weighted(FAKE, 1, FAKE, FAKE, FAKE + 2, 4, 8, 2, 2, 1, FAKE, None, None) == 2
     assert lib.moe_padded_gather_weighted(FAKE, 0, FAKE, FAKE, None, FAKE, 4, 8, 2, 1, FAKE, 8, None, None) == 1
     assert lib.moe_padded_gather_weighted(FAKE, 0, FAKE, FAKE, FAKE, None, 4, 8, 2, 1, FAKE, 8, None, None) == 1
+    # gating: top_k above E, bad mode, E above the gating limit
+    assert lib.moe_topk_gating(FAKE, 4, 8, 9, 0, 1, FAKE, FAKE, None) == 1
+    assert lib.moe_topk_gating(FAKE, 4, 8, 2, 5, 1, FAKE, FAKE, None) == 1
+    assert lib.moe_topk_gating(FAKE, 4, 2048, 2, 0, 1, FAKE, FAKE, None) == 2
+    assert lib.moe_topk_gating(FAKE, 0, 8, 2, 1, 0, FAKE, FAKE, None) == 0
     assert lib.moe_routing_map_to_indices_fwd(FAKE, FAKE, -1, 4, 2, FAKE, FAKE, None) == 1
     assert lib.moe_routing_map_to_indices_fwd(FAKE, FAKE, 4, 4, 0, FAKE, FAKE, None) == 1
     assert lib.moe_routing_map_to_indices_fwd(FAKE + 1, FAKE, 4, 4, 2, FAKE, FAKE, None) == 2

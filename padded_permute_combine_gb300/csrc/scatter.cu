@@ -10,9 +10,12 @@
 // atomics are needed. A slot finds its expert row through the inverse
 // permutation `positions`; slots dropped by capacity are compacted away
 // (ballot + __fns keeps slot order), and the loads of up to eight kept slots
-// are issued before they are summed, to keep bytes in flight. Sums use
-// Blackwell's packed f32x2 add, still rounding each operation to nearest,
-// so the result is bit-identical to the scalar sequence.
+// are issued before they are summed, to keep bytes in flight. For 16-byte
+// rows with top_k <= 8 the chunks travel by cp.async into a per-warp
+// shared-memory ring instead of registers (scatter_async_kernel), which lets
+// more warps per SM keep more bytes in flight. Sums use Blackwell's packed
+// f32x2 add, still rounding each operation to nearest, so the result is
+// bit-identical to the scalar sequence.
 #include "common.cuh"
 #include "vec_math.cuh"
 
@@ -279,6 +282,102 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) scatter_kernel(ScatterAr
   }
 }
 
+// ---------------------------------------------------------------------------
+// Asynchronous-copy variant (16-byte rows, 32-bit offsets, top_k <= 8): the
+// kept rows' chunks are copied global -> shared with cp.async into a
+// per-warp ring of kAsyncSlots 512-byte slots, so the bytes in flight do not
+// occupy registers. A lane copies, and later reads back, only its own 16
+// bytes of every slot, so the only synchronisation is the lane's own
+// cp.async.wait_group. Chunks in flight per warp: kAsyncSlots / KQ, i.e.
+// 8, 4 or 2 for at most 2, 4 or 8 kept rows.
+
+constexpr int kAsyncThreads = 128;
+constexpr int kAsyncWarps = kAsyncThreads / kWarp;
+constexpr int kAsyncSlots = 16;
+
+__device__ __forceinline__ void cp_async16(void* smem, const void* gmem) {
+  const unsigned s = (unsigned)__cvta_generic_to_shared(smem);
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(s), "l"(gmem) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
+template <int KQ, typename ET, bool WEIGHTED>
+__device__ __forceinline__ void stream_kept_async(const uint4* __restrict__ xe, uint4* __restrict__ dst, uint4* ring,
+                                                  const uint32_t (&off)[8], const float (&w)[8], int nk,
+                                                  int64_t c_begin, int64_t c_end, int lane) {
+  constexpr int DC = kAsyncSlots / KQ;  // chunks in flight
+  const int64_t nch = (c_end - c_begin + kWarp - 1) / kWarp;
+  auto issue = [&](int64_t j) {
+    const int64_t c = c_begin + j * kWarp + lane;
+    if (j < nch && c < c_end) {
+      uint4* slot = ring + (int)(j % DC) * KQ * kWarp + lane;
+#pragma unroll
+      for (int q = 0; q < KQ; ++q)
+        if (q < nk) cp_async16(slot + q * kWarp, xe + c + off[q]);
+    }
+    cp_async_commit();  // possibly empty: keeps one group per chunk
+  };
+#pragma unroll
+  for (int d = 0; d < DC - 1; ++d) issue(d);
+  for (int64_t j = 0; j < nch; ++j) {
+    issue(j + DC - 1);
+    cp_async_wait<DC - 1>();  // this lane's copies of chunk j have landed
+    const int64_t c = c_begin + j * kWarp + lane;
+    if (c < c_end) {
+      const uint4* slot = ring + (int)(j % DC) * KQ * kWarp + lane;
+      uint4 v[KQ];
+#pragma unroll
+      for (int q = 0; q < KQ; ++q)
+        if (q < nk) v[q] = slot[q * kWarp];
+      sum_store<KQ, 16, ET, WEIGHTED>(v, w, nk, dst + c);
+    }
+  }
+  cp_async_wait<0>();
+}
+
+// Binned tokens keep few rows (2 to 5 of 8 at the DeepSeek-V3 batch), so
+// more resident warps pay: the binned kernel is held to 80 registers (6 CTAs
+// per SM); the padded one (8 rows per token) measured faster without the cap.
+template <typename ET, bool PADDED, bool WEIGHTED>
+__global__ void __launch_bounds__(kAsyncThreads, PADDED ? 1 : 6) scatter_async_kernel(ScatterArgs g) {
+  __shared__ uint4 ring_all[kAsyncWarps * kAsyncSlots * kWarp];
+  const int lane = lane_id();
+  uint4* ring = ring_all + (threadIdx.x / kWarp) * kAsyncSlots * kWarp;
+  const int64_t warps = (int64_t)gridDim.x * kAsyncWarps;
+  const int64_t items = g.T * g.segs;
+  const uint4* __restrict__ xe = reinterpret_cast<const uint4*>(g.xe);
+  uint4* __restrict__ out = reinterpret_cast<uint4*>(g.out);
+  for (int64_t item = (int64_t)blockIdx.x * kAsyncWarps + threadIdx.x / kWarp; item < items; item += warps) {
+    const int64_t t = item / g.segs;
+    const int64_t c_begin = (item - t * g.segs) * g.seg_vecs;
+    const int64_t c_end = min(c_begin + g.seg_vecs, g.vecs);
+    int64_t row = -1;
+    float wt = 1.0f;
+    if (lane < g.top_k) {
+      const int64_t a = t * g.top_k + lane;
+      row = slot_row<PADDED>(g, a);
+      if (WEIGHTED) wt = __ldg(g.weights + a);
+    }
+    const int nk = compact_kept(row, wt);
+    uint32_t off[8];
+    float w[8];
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+      const int64_t r = __shfl_sync(0xffffffffu, row, q);
+      off[q] = (uint32_t)((r < 0 ? 0 : r) * g.vecs);
+      w[q] = __shfl_sync(0xffffffffu, wt, q);
+    }
+    uint4* dst = out + t * g.vecs;
+    if (nk <= 2) stream_kept_async<2, ET, WEIGHTED>(xe, dst, ring, off, w, nk, c_begin, c_end, lane);
+    else if (nk <= 4) stream_kept_async<4, ET, WEIGHTED>(xe, dst, ring, off, w, nk, c_begin, c_end, lane);
+    else stream_kept_async<8, ET, WEIGHTED>(xe, dst, ring, off, w, nk, c_begin, c_end, lane);
+  }
+}
+
 __global__ void invert_kernel(const int32_t* __restrict__ indices, int64_t n, int32_t* __restrict__ positions,
                               int32_t* status) {
   for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x) {
@@ -295,6 +394,19 @@ int launch_scatter(ScatterArgs g, cudaStream_t s) {
   g.seg_vecs = ((g.vecs + g.segs - 1) / g.segs + kWarp - 1) / kWarp * kWarp;
   g.segs = (g.vecs + g.seg_vecs - 1) / g.seg_vecs;
   g.offsets32 = (uint64_t)g.xe_rows * (uint64_t)g.vecs <= 0xffffffffull;
+  if constexpr (VB == 16) {
+    if (g.offsets32 && g.top_k <= kKeptInFlight) {
+      const int64_t actas = (g.T * g.segs + kAsyncWarps - 1) / kAsyncWarps;
+      if (g.weights != nullptr) {
+        auto k = scatter_async_kernel<ET, PADDED, true>;
+        k<<<persistent_grid(k, kAsyncThreads, 0, actas), kAsyncThreads, 0, s>>>(g);
+      } else {
+        auto k = scatter_async_kernel<ET, PADDED, false>;
+        k<<<persistent_grid(k, kAsyncThreads, 0, actas), kAsyncThreads, 0, s>>>(g);
+      }
+      return check_launch();
+    }
+  }
   const int64_t work_ctas = (g.T * g.segs + (kThreads / kWarp) - 1) / (kThreads / kWarp);
   if (g.weights != nullptr) {
     auto k = scatter_kernel<VB, ET, PADDED, true>;

@@ -42,6 +42,10 @@ METRIC = "routed rows/sec and achieved HBM GB/s (% of GB300 peak), gather+scatte
 UNIT = "rows/s"
 L2_FLUSH_BYTES = 512 << 20
 FALLBACK_HBM_GBS = 6800.0
+# the csrc/ translation unit each timed kernel is compiled from
+KERNEL_UNIT = {"compaction_fwd": "compaction", "compaction_bwd": "compaction", "route_build": "route_build",
+               "binned_gather": "gather", "padded_gather": "gather", "binned_scatter": "scatter",
+               "padded_scatter": "scatter", "binned_wgrad": "wgrad", "padded_wgrad": "wgrad"}
 
 
 def parse():
@@ -92,7 +96,8 @@ def measured_peak():
 
 def traffic_from_profiles(kernel: str, digest: str):
     """dram read+write bytes per launch of `kernel`, from the committed ncu
-    summary, if it was taken on the current sources."""
+    summary, if it was taken on the kernel's current sources (`digest` is
+    the hash of its translation unit and the shared headers)."""
     path = os.path.join(ROOT, "profiles", "dram_traffic.txt")
     try:
         for line in open(path):
@@ -388,7 +393,7 @@ def run_gpu(args, rank, world, local_rank):
         "kernels": kern,
         "roofline": {"bound": "hbm", "kernel": dominant, "achieved": ach, "peak": peak, "peak_kind": peak_kind,
                      "unit": "GB/s", "frac": round(ach / peak, 4),
-                     "traffic": traffic_from_profiles(dominant, libbuild.source_digest())},
+                     "traffic": traffic_from_profiles(dominant, libbuild.kernel_digest(KERNEL_UNIT[dominant]))},
         "e2e": e2e,
         "next_rows": next_rows,
         "gpu_launches": sum(l for _, l, _ in ops) * args.steps,

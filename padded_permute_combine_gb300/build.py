@@ -48,6 +48,21 @@ def source_digest() -> str:
     return h.hexdigest()[:16]
 
 
+def kernel_digest(unit: str) -> str:
+    """Hash of one kernel family's translation unit (``csrc/<unit>.cu``), the
+    shared headers and the compile flags: it changes only when what that
+    kernel is compiled from changes, so a profile taken on it stays valid
+    while other kernels are edited."""
+    h = hashlib.sha256()
+    files = [os.path.join(CSRC, unit + ".cu")] + sorted(glob.glob(os.path.join(CSRC, "*.cuh")))
+    for f in files:
+        h.update(os.path.basename(f).encode())
+        with open(f, "rb") as fh:
+            h.update(fh.read())
+    h.update(" ".join(ARCH + NVCC_FLAGS[:-4]).encode())
+    return h.hexdigest()[:16]
+
+
 def _compile(src: str, extra: list[str]) -> tuple[str, str]:
     obj = os.path.join(BUILD_DIR, os.path.basename(src)[:-3] + ".o")
     cmd = [_nvcc(), *ARCH, *NVCC_FLAGS, *extra, "-c", src, "-o", obj]

@@ -69,6 +69,29 @@ __device__ __forceinline__ uint16_t ld_stream(const uint16_t* p) {
   return v;
 }
 
+// 256-bit loads with an L2 eviction priority: ld_keep marks the lines
+// evict-last (rows re-read by later warps: token rows of the gather, gradient
+// rows of wgrad), ld_once evict-first (rows read exactly once). Narrower
+// vectors take ld_stream.
+__device__ __forceinline__ u32x8 ld_keep(const u32x8* p) {
+  u32x8 v;
+  asm volatile("ld.global.nc.L1::no_allocate.L2::evict_last.v8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+               : "=r"(v.w[0]), "=r"(v.w[1]), "=r"(v.w[2]), "=r"(v.w[3]), "=r"(v.w[4]), "=r"(v.w[5]), "=r"(v.w[6]),
+                 "=r"(v.w[7])
+               : "l"(p));
+  return v;
+}
+__device__ __forceinline__ u32x8 ld_once(const u32x8* p) {
+  u32x8 v;
+  asm volatile("ld.global.nc.L1::no_allocate.L2::evict_first.v8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+               : "=r"(v.w[0]), "=r"(v.w[1]), "=r"(v.w[2]), "=r"(v.w[3]), "=r"(v.w[4]), "=r"(v.w[5]), "=r"(v.w[6]),
+                 "=r"(v.w[7])
+               : "l"(p));
+  return v;
+}
+template <typename V> __device__ __forceinline__ V ld_keep(const V* p) { return ld_stream(p); }
+template <typename V> __device__ __forceinline__ V ld_once(const V* p) { return ld_stream(p); }
+
 // Store of write-once output: evict-first so it does not push reused inputs out of L2.
 __device__ __forceinline__ void st_stream(u32x8* p, const u32x8& v) {
   asm volatile("st.global.cs.v8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"l"(p), "r"(v.w[0]), "r"(v.w[1]),

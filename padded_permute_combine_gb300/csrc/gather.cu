@@ -8,7 +8,8 @@
 // copy of its source token row or as zeros (unused capacity / padding), so no
 // separate clearing pass is needed. One warp owns one output row at a time
 // and streams it with VB-byte vectors (256-bit loads and stores when the row
-// and pointers allow), U vectors per lane in flight. The bin
+// and pointers allow), U vectors per lane in flight; token rows are loaded
+// evict-last, because up to TOP_K output rows copy the same token. The bin
 // vectors are staged in shared memory; a padded row finds its expert by
 // binary search over padded_bins. The weighted variant (the gradient of the
 // combine with respect to the expert rows, d row(a) = w[a] * dy[a / TOP_K])
@@ -144,7 +145,7 @@ __global__ void __launch_bounds__(kThreads) gather_kernel(GatherArgs g) {
 #pragma unroll
         for (int u = 0; u < U; ++u) {
           const int64_t c = c0 + u * kWarp + lane;
-          if (c < g.vecs) v[u] = ld_stream(s + c);
+          if (c < g.vecs) v[u] = ld_keep(s + c);
         }
 #pragma unroll
         for (int u = 0; u < U; ++u) {

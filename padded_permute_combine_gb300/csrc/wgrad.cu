@@ -138,8 +138,8 @@ __global__ void __launch_bounds__(kThreads) wgrad_kernel(WgradArgs g) {
       for (int u = 0; u < U; ++u) {
         const int64_t c = c0 + u * kWarp + lane;
         if (c < g.vecs) {
-          vx[u] = ld_stream(xr + c);
-          vg[u] = ld_stream(gv + c);
+          vx[u] = ld_once(xr + c);  // each expert row is read once
+          vg[u] = ld_keep(gv + c);  // the token's gradient row, once per kept slot
         }
       }
 #pragma unroll

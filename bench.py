@@ -176,8 +176,18 @@ class Path:
         torch.cuda.synchronize(dev)
         self.P = int(self.route.padded_bins[-1].item())
         self.xp = torch.empty((self.P, H), dtype=bf, device=dev)
-        counts = np.diff(np.concatenate([[0], self.route.bins.cpu().numpy()]))
-        self.kept = int(np.minimum(counts, r.capacity).sum())
+        self.counts = np.diff(np.concatenate([[0], self.route.bins.cpu().numpy()]))
+        self.kept = int(np.minimum(self.counts, r.capacity).sum())
+        self.kept_tokens = self.tokens_with_kept_slot(r.capacity)
+
+    def tokens_with_kept_slot(self, capacity: int) -> int:
+        """Tokens with at least one assignment inside `capacity` (each such
+        token's gradient row is read once by wgrad)."""
+        bins = self.route.bins.cpu().numpy().astype(np.int64)
+        idx = self.route.indices.cpu().numpy().astype(np.int64)
+        start = np.concatenate([[0], bins[:-1]])
+        rank = np.arange(idx.size) - np.repeat(start, bins - start)
+        return int(np.unique(idx[rank < capacity] // self.r.K).size)
 
     def front(self):
         p, r = self.p, self.r
@@ -193,18 +203,18 @@ class Path:
             ("compaction_fwd", 1, lambda: p.moe_routing_map_to_indices_fwd(self.probs, self.rmap, K,
                                                                            out=(self.pi, self.idx))),
             ("route_build", 3, lambda: p.moe_route_build(self.idx, E, r.pad_multiple, workspace=self.ws, out=rt)),
-            ("binned_gather", 1, lambda: p.moe_binned_gather(self.x, rt.indices, rt.bins, E, r.capacity, K,
+            ("binned_gather", 3, lambda: p.moe_binned_gather(self.x, rt.indices, rt.bins, E, r.capacity, K,
                                                              out=self.xb)),
             ("binned_scatter", 1, lambda: p.moe_binned_scatter(self.xb, rt.indices, rt.bin_ids, rt.bins, w, T, K,
                                                                positions=rt.positions, out=self.yb)),
             ("binned_wgrad", 1, lambda: p.moe_binned_wgrad(self.xb, self.grad, rt.indices, rt.bin_ids, rt.bins, K,
                                                            out=self.wgb)),
-            ("padded_gather", 1, lambda: p.moe_padded_gather(self.x, rt.indices, rt.bins, rt.padded_bins, K,
+            ("padded_gather", 3, lambda: p.moe_padded_gather(self.x, rt.indices, rt.bins, rt.padded_bins, K,
                                                              out_rows=self.P, out=self.xp)),
             ("padded_scatter", 1, lambda: p.moe_padded_scatter(self.xp, rt.indices, rt.bin_ids, rt.bins,
                                                                rt.padded_bins, w, T, K, positions=rt.positions,
                                                                out=self.yp)),
-            ("padded_wgrad", 1, lambda: p.moe_padded_wgrad(self.xp, self.grad, rt.indices, rt.bin_ids, rt.bins,
+            ("padded_wgrad", 2, lambda: p.moe_padded_wgrad(self.xp, self.grad, rt.indices, rt.bin_ids, rt.bins,
                                                            rt.padded_bins, K, out=self.wgp)),
             ("compaction_bwd", 1, lambda: p.moe_routing_map_to_indices_bwd(self.wgp.view(T, K), self.idx, E,
                                                                            out=self.gprobs)),
@@ -229,27 +239,30 @@ class Path:
              T * E * 4 + T * K * 8),
             ("binned_gather_weighted",
              lambda: p.moe_binned_gather_weighted(self.grad, rt.indices, rt.bins, w, E, r.capacity, K, out=self.gwb),
-             self.kept * H * b + E * r.capacity * H * b + 8 * self.kept + 4 * E),
+             self.kept_tokens * H * b + E * r.capacity * H * b + 8 * n + 4 * E),
             ("padded_gather_weighted",
              lambda: p.moe_padded_gather_weighted(self.grad, rt.indices, rt.bins, rt.padded_bins, w, K,
                                                   out_rows=self.P, out=self.gwp),
-             n * H * b + self.P * H * b + 8 * n + 8 * E),
+             T * H * b + self.P * H * b + 8 * n + 8 * E),
         ]
 
     def algorithmic_bytes(self) -> dict:
-        """Bytes each kernel must move (no reuse credited), per launch."""
+        """Bytes each kernel must move at least, per launch: every token row,
+        expert row and output row that the operation touches, once, plus its
+        index vectors read once (a row that several slots share, such as the
+        token row a gather copies TOP_K times, counts once)."""
         r = self.r
         T, H, E, K, n, b = r.T, r.H, r.E, r.K, self.n, 2
-        kept, P, cap = self.kept, self.P, r.capacity
+        kept, P, cap, Tk = self.kept, self.P, r.capacity, self.kept_tokens
         return {
             "compaction_fwd": T * E + T * K * 4 + T * K * 8,
             "route_build": 2 * 4 * n + 12 * n + 8 * E,
-            "binned_gather": kept * H * b + E * cap * H * b + 4 * kept + 4 * E,
+            "binned_gather": Tk * H * b + E * cap * H * b + 4 * n + 4 * E,
             "binned_scatter": kept * H * b + T * H * b + 12 * n + 4 * E,
-            "binned_wgrad": 2 * kept * H * b + 12 * n + 4 * E,
-            "padded_gather": n * H * b + P * H * b + 4 * n + 8 * E,
+            "binned_wgrad": kept * H * b + Tk * H * b + 12 * n + 4 * E,
+            "padded_gather": T * H * b + P * H * b + 4 * n + 8 * E,
             "padded_scatter": n * H * b + T * H * b + 12 * n + 8 * E,
-            "padded_wgrad": 2 * n * H * b + 12 * n + 8 * E,
+            "padded_wgrad": n * H * b + T * H * b + 12 * n + 8 * E,
             "compaction_bwd": T * K * 8 + T * E * 4,
         }
 
@@ -414,28 +427,89 @@ def time_next_rows(args, path, flush, stream):
     every launch, CUDA events on the launching stream)."""
     import torch
 
-    peak, peak_kind = measured_peak()
     out = {}
-    reps = max(3, min(args.steps, 50))
     for name, fn, nbytes in path.next_ops():
-        for _ in range(3):
-            flush.zero_()
-            fn()
-        ms = []
-        for _ in range(reps):
-            flush.zero_()
-            a = torch.cuda.Event(enable_timing=True)
-            b = torch.cuda.Event(enable_timing=True)
-            a.record(stream)
-            fn()
-            b.record(stream)
-            b.synchronize()
-            ms.append(a.elapsed_time(b))
-        mean = statistics.mean(ms)
-        gbs = nbytes / (mean * 1e-3) / 1e9
-        out[name] = {"ms": round(mean, 5), "algorithmic_bytes": nbytes, "gbs": round(gbs, 1),
-                     "frac_of_%s_peak" % peak_kind: round(gbs / peak, 4)}
+        out[name] = time_alone(args, fn, nbytes, flush, stream)
+    out.update(time_sweeps(args, path, flush, stream))
     return out
+
+
+def time_alone(args, fn, nbytes, flush, stream) -> dict:
+    """Mean CUDA-event time of `fn` on `stream` over up to 50 launches, each
+    after an L2 flush, and its algorithmic bandwidth."""
+    import torch
+
+    peak, peak_kind = measured_peak()
+    reps = max(3, min(args.steps, 50))
+    for _ in range(3):
+        flush.zero_()
+        fn()
+    ms = []
+    for _ in range(reps):
+        flush.zero_()
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        fn()
+        b.record(stream)
+        b.synchronize()
+        ms.append(a.elapsed_time(b))
+    mean = statistics.mean(ms)
+    gbs = nbytes / (mean * 1e-3) / 1e9
+    return {"ms": round(mean, 5), "algorithmic_bytes": nbytes, "gbs": round(gbs, 1),
+            "frac_of_%s_peak" % peak_kind: round(gbs / peak, 4)}
+
+
+def time_sweeps(args, path, flush, stream) -> dict:
+    """The binned kernels of the same batch at capacity factors 0.5, 1.25 and
+    2.0 (capacity = ceil(f*T*K/E)), and the padded kernels at padding
+    multiples 16, 64 and 256 (route build rerun for each multiple), each
+    launch timed alone."""
+    import torch
+
+    p, r, rt = path.p, path.r, path.route
+    T, H, E, K, n, b = r.T, r.H, r.E, r.K, path.n, 2
+    bf, dev = torch.bfloat16, path.dev
+    w = path.pi.view(-1)
+    y = torch.empty((T, H), dtype=bf, device=dev)
+    wg = torch.empty(n, dtype=torch.float32, device=dev)
+    caps = {}
+    for cf in (0.5, 1.25, 2.0):
+        cap = math.ceil(cf * T * K / E)
+        kept = int(np.minimum(path.counts, cap).sum())
+        xb = torch.empty((E, cap, H), dtype=bf, device=dev)
+        ops = [
+            ("binned_gather", lambda: p.moe_binned_gather(path.x, rt.indices, rt.bins, E, cap, K, out=xb),
+             path.tokens_with_kept_slot(cap) * H * b + E * cap * H * b + 4 * n + 4 * E),
+            ("binned_scatter", lambda: p.moe_binned_scatter(xb, rt.indices, rt.bin_ids, rt.bins, w, T, K,
+                                                            positions=rt.positions, out=y),
+             kept * H * b + T * H * b + 12 * n + 4 * E),
+            ("binned_wgrad", lambda: p.moe_binned_wgrad(xb, path.grad, rt.indices, rt.bin_ids, rt.bins, K, out=wg),
+             kept * H * b + path.tokens_with_kept_slot(cap) * H * b + 12 * n + 4 * E)]
+        caps[str(cf)] = {"capacity": cap, "kept": kept}
+        caps[str(cf)].update({name: time_alone(args, fn, nb, flush, stream) for name, fn, nb in ops})
+        del xb
+    pads = {}
+    for m in (16, 64, 256):
+        rm = p.Route(*(torch.empty_like(t) for t in rt))
+        p.moe_route_build(path.idx, E, m, workspace=path.ws, out=rm)
+        torch.cuda.synchronize(dev)
+        P = int(rm.padded_bins[-1].item())
+        xp = torch.empty((P, H), dtype=bf, device=dev)
+        ops = [
+            ("padded_gather", lambda: p.moe_padded_gather(path.x, rm.indices, rm.bins, rm.padded_bins, K,
+                                                          out_rows=P, out=xp),
+             T * H * b + P * H * b + 4 * n + 8 * E),
+            ("padded_scatter", lambda: p.moe_padded_scatter(xp, rm.indices, rm.bin_ids, rm.bins, rm.padded_bins, w,
+                                                            T, K, positions=rm.positions, out=y),
+             n * H * b + T * H * b + 12 * n + 8 * E),
+            ("padded_wgrad", lambda: p.moe_padded_wgrad(xp, path.grad, rm.indices, rm.bin_ids, rm.bins,
+                                                        rm.padded_bins, K, out=wg),
+             n * H * b + T * H * b + 12 * n + 8 * E)]
+        pads[str(m)] = {"padded_rows": P}
+        pads[str(m)].update({name: time_alone(args, fn, nb, flush, stream) for name, fn, nb in ops})
+        del xp
+    return {"capacity_factor_sweep": caps, "pad_multiple_sweep": pads}
 
 
 def run_e2e(args, path, dev, dist):

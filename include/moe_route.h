@@ -155,6 +155,14 @@ int moe_route_build_noalloc(const int32_t* top_expert, int64_t n,
  *   x    [T, H] dtype;  out [E, capacity, H] dtype (fully written).
  *   indices [n], bins [E] from moe_route_build; n = T*top_k.
  * capacity >= 0; capacity == 0 writes nothing.
+ * Schedule (the result does not depend on it): when out holds more than
+ * 4n bytes plus one row, the gather first stores the inverse permutation of
+ * indices in the last 4n bytes of out (16-byte aligned), then copies each
+ * token row once to all of its kept rows, then writes the rows that overlap
+ * those bytes; three launches, no workspace. out must not alias any input.
+ * A sorted position that does not map back to its assignment (indices not a
+ * permutation) sets MOE_STATUS_BAD_INDEX; bins that decrease or pass n set
+ * MOE_STATUS_BAD_BINS. The same holds for every gather below.
  */
 int moe_binned_gather(const void* x, int32_t dtype, const int32_t* indices,
                       const int32_t* bins, int64_t num_tokens, int64_t hidden,
@@ -246,6 +254,15 @@ int moe_padded_scatter(const void* xe, int32_t dtype, const int32_t* indices,
  * Accumulated in fp32 with compensated (error-free transformation)
  * summation, so the result is close to the correctly rounded dot.
  *   xe as for scatter; grad [T, H] dtype; wgrad [n] fp32 (fully written).
+ * No workspace. moe_padded_wgrad takes two launches: the first stores the
+ * inverse permutation of indices in wgrad itself (n 32-bit slots), the
+ * second reads each slot once and overwrites it with the result, visiting
+ * assignments in id order so that each gradient row is read about once.
+ * moe_binned_wgrad is one launch over sorted positions. wgrad must not
+ * alias any input; its contents are meaningful only once the call's work
+ * has run. In the padded call a position that does not map back to its
+ * assignment (indices not a permutation) sets MOE_STATUS_BAD_INDEX and that
+ * slot's result is 0.
  */
 int moe_binned_wgrad(const void* xe, const void* grad, int32_t dtype,
                      const int32_t* indices, const int32_t* bin_ids,

@@ -92,6 +92,21 @@ __device__ __forceinline__ u32x8 ld_once(const u32x8* p) {
 template <typename V> __device__ __forceinline__ V ld_keep(const V* p) { return ld_stream(p); }
 template <typename V> __device__ __forceinline__ V ld_once(const V* p) { return ld_stream(p); }
 
+// Read-only load that allocates in L1: for rows that neighbouring warps of
+// the same CTA read at about the same time.
+__device__ __forceinline__ u32x8 ld_l1(const u32x8* p) {
+  u32x8 v;
+  asm volatile("ld.global.nc.v8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+               : "=r"(v.w[0]), "=r"(v.w[1]), "=r"(v.w[2]), "=r"(v.w[3]), "=r"(v.w[4]), "=r"(v.w[5]), "=r"(v.w[6]),
+                 "=r"(v.w[7])
+               : "l"(p));
+  return v;
+}
+__device__ __forceinline__ uint4 ld_l1(const uint4* p) { return __ldg(p); }
+__device__ __forceinline__ uint2 ld_l1(const uint2* p) { return __ldg(p); }
+__device__ __forceinline__ uint32_t ld_l1(const uint32_t* p) { return __ldg(reinterpret_cast<const unsigned int*>(p)); }
+__device__ __forceinline__ uint16_t ld_l1(const uint16_t* p) { return __ldg(reinterpret_cast<const unsigned short*>(p)); }
+
 // Store of write-once output: evict-first so it does not push reused inputs out of L2.
 __device__ __forceinline__ void st_stream(u32x8* p, const u32x8& v) {
   asm volatile("st.global.cs.v8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"l"(p), "r"(v.w[0]), "r"(v.w[1]),

@@ -4,16 +4,23 @@
 //  "Build Triton-Ascend Padded MoE Routing": Goal, Workflow steps 4-5,
 //  Implementation Pattern, Guardrails).
 //
-// Destination-major: every output row is produced exactly once, either as a
-// copy of its source token row or as zeros (unused capacity / padding), so no
-// separate clearing pass is needed. One warp owns one output row at a time
-// and streams it with VB-byte vectors (256-bit loads and stores when the row
-// and pointers allow), U vectors per lane in flight; token rows are loaded
-// evict-last, because up to TOP_K output rows copy the same token. The bin
-// vectors are staged in shared memory; a padded row finds its expert by
-// binary search over padded_bins. The weighted variant (the gradient of the
-// combine with respect to the expert rows, d row(a) = w[a] * dy[a / TOP_K])
-// scales each copied row by its assignment's weight on the way through.
+// Every output row is produced exactly once, as a copy of its source token
+// row or as zeros (unused capacity / padding), so no clearing pass is
+// needed. Two schedules:
+//  - token-major (the usual case, see "token-major path" below): one warp
+//    reads a token row once and writes it to each of the token's kept
+//    output rows, so x leaves HBM once instead of once per kept slot;
+//  - destination-major (gather_kernel; tiny outputs, and the last few rows
+//    of the token-major schedule): one warp owns one output row, finds its
+//    source assignment through bins and indices (a padded row finds its
+//    expert by binary search over padded_bins) and streams the row; token
+//    rows are loaded evict-last there, as up to TOP_K rows copy the same
+//    token.
+// Rows move as VB-byte vectors (256-bit loads and stores when the row and
+// pointers allow) with U vectors per lane in flight; the bin vectors are
+// staged in shared memory. The weighted variant (the gradient of the combine
+// with respect to the expert rows, d row(a) = w[a] * dy[a / TOP_K]) scales
+// each copied row by its assignment's weight on the way through.
 #include "common.cuh"
 #include "vec_math.cuh"
 
@@ -39,6 +46,9 @@ struct GatherArgs {
   int32_t capacity;
   int32_t top_k;
   int32_t* status;
+  int64_t T = 0;
+  int64_t row_begin = 0;              // first row the destination-major kernel writes
+  const int32_t* positions = nullptr;  // token-major path: inverse of indices, in the tail of out
 };
 
 // Assignment id whose token fills output row `row`, or -1 for a zero row.
@@ -132,8 +142,8 @@ __global__ void __launch_bounds__(kThreads) gather_kernel(GatherArgs g) {
   const int64_t warps = (int64_t)gridDim.x * (blockDim.x / kWarp);
   const V* __restrict__ x = reinterpret_cast<const V*>(g.x);
   V* __restrict__ out = reinterpret_cast<V*>(g.out);
-  for (int64_t row = (int64_t)blockIdx.x * (blockDim.x / kWarp) + threadIdx.x / kWarp; row < g.rows_out;
-       row += warps) {
+  for (int64_t row = g.row_begin + (int64_t)blockIdx.x * (blockDim.x / kWarp) + threadIdx.x / kWarp;
+       row < g.rows_out; row += warps) {
     const int64_t a = source_assignment<PADDED>(g, sb, spb, row);
     V* dst = out + row * g.vecs;
     if (a >= 0) {
@@ -164,13 +174,201 @@ __global__ void __launch_bounds__(kThreads) gather_kernel(GatherArgs g) {
   }
 }
 
+// ------------------------------------------------------- token-major path
+//
+// When the output is larger than n int32 values (every realistic shape), the
+// gather reads each token row once: (1) the inverse permutation of indices is
+// written into the last bytes of `out` itself, so no workspace is needed;
+// (2) one warp per token resolves the token's TOP_K slots to output rows
+// through it and copies the token row to every kept row, and the same launch
+// zero-fills the unused rows; (3) the few rows that overlap the borrowed
+// tail are then produced destination-major by gather_kernel, overwriting it.
+
+__global__ void positions_kernel(const int32_t* __restrict__ indices, int64_t n, int32_t* __restrict__ positions,
+                                 int32_t* status) {
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x) {
+    const int32_t a = __ldg(indices + i);
+    if (a >= 0 && a < n) positions[a] = (int32_t)i;
+    else flag_status(status, MOE_STATUS_BAD_INDEX);
+  }
+}
+
+// Output row of sorted position i, or -1 when capacity drops it (or the
+// bins are inconsistent with it, which is flagged).
+template <bool PADDED>
+__device__ __forceinline__ int64_t position_row(const GatherArgs& g, const int32_t* sb, const int32_t* spb,
+                                                int64_t i) {
+  int lo = 0, hi = g.E - 1;  // first expert whose inclusive end exceeds i
+  while (lo < hi) {
+    const int mid = (lo + hi) >> 1;
+    if (sb[mid] > i) hi = mid; else lo = mid + 1;
+  }
+  const int64_t start = lo > 0 ? sb[lo - 1] : 0;
+  const int64_t j = i - start;
+  if (sb[lo] <= i || j < 0) {
+    flag_status(g.status, MOE_STATUS_BAD_BINS);
+    return -1;
+  }
+  if (!PADDED) return j < g.capacity ? (int64_t)lo * g.capacity + j : -1;
+  const int64_t pstart = lo > 0 ? spb[lo - 1] : 0;
+  if (j >= (int64_t)spb[lo] - pstart) {
+    flag_status(g.status, MOE_STATUS_BAD_BINS);
+    return -1;
+  }
+  if (pstart + j >= g.rows_out) {
+    flag_status(g.status, MOE_STATUS_ROWS_MISMATCH);
+    return -1;
+  }
+  return pstart + j;
+}
+
+// Whether output row r receives no token (unused capacity or padding).
+template <bool PADDED>
+__device__ __forceinline__ bool is_zero_row(const GatherArgs& g, const int32_t* sb, const int32_t* spb, int64_t r) {
+  int32_t e;
+  int64_t j;
+  if (!PADDED) {
+    e = (int32_t)(r / g.capacity);
+    j = r - (int64_t)e * g.capacity;
+  } else {
+    if (r >= spb[g.E - 1]) return true;
+    int lo = 0, hi = g.E - 1;
+    while (lo < hi) {
+      const int mid = (lo + hi) >> 1;
+      if (spb[mid] > r) hi = mid; else lo = mid + 1;
+    }
+    e = lo;
+    j = r - (e > 0 ? spb[e - 1] : 0);
+  }
+  return j >= (int64_t)sb[e] - (e > 0 ? sb[e - 1] : 0);
+}
+
+template <int VB, int U, bool PADDED, typename ST>
+__global__ void __launch_bounds__(kThreads) gather_token_kernel(GatherArgs g) {
+  constexpr bool kWeighted = !std::is_void<ST>::value;
+  constexpr int KQ = 8;  // kept slots whose rows are written per sweep of the token row
+  constexpr unsigned kAll = 0xffffffffu;
+  using V = typename Vec<VB>::T;
+  __shared__ int32_t sbins[kStageMax];
+  __shared__ int32_t spbins[PADDED ? kStageMax : 1];
+  const bool staged = g.E <= kStageMax;
+  if (staged) {
+    for (int e = threadIdx.x; e < g.E; e += blockDim.x) {
+      sbins[e] = __ldg(g.bins + e);
+      if (PADDED) spbins[e] = __ldg(g.padded_bins + e);
+    }
+    __syncthreads();
+  }
+  const int32_t* sb = staged ? sbins : g.bins;
+  const int32_t* spb = PADDED ? (staged ? spbins : g.padded_bins) : nullptr;
+  if (blockIdx.x == 0) {
+    // bins nondecreasing, ending at most at n; padded segments hold their counts
+    for (int e = threadIdx.x; e < g.E; e += blockDim.x) {
+      const int32_t prev = e > 0 ? sb[e - 1] : 0;
+      bool ok = sb[e] >= prev && (e < g.E - 1 || sb[e] <= g.n);
+      if (PADDED) ok = ok && (int64_t)spb[e] - (e > 0 ? spb[e - 1] : 0) >= (int64_t)sb[e] - prev;
+      if (!ok) flag_status(g.status, MOE_STATUS_BAD_BINS);
+    }
+  }
+
+  const int lane = lane_id();
+  const int64_t warps = (int64_t)gridDim.x * (blockDim.x / kWarp);
+  const V* __restrict__ x = reinterpret_cast<const V*>(g.x);
+  V* __restrict__ out = reinterpret_cast<V*>(g.out);
+  const int64_t items = g.T + g.row_begin;  // tokens, then the rows this kernel may zero-fill
+  for (int64_t item = (int64_t)blockIdx.x * (blockDim.x / kWarp) + threadIdx.x / kWarp; item < items;
+       item += warps) {
+    if (item >= g.T) {
+      const int64_t r = item - g.T;
+      if (is_zero_row<PADDED>(g, sb, spb, r)) {
+        V* dst = out + r * g.vecs;
+        const V z = zero_vec<V>();
+        for (int64_t c = lane; c < g.vecs; c += kWarp) st_stream(dst + c, z);
+      }
+      continue;
+    }
+    const V* src = x + item * g.vecs;
+    for (int k0 = 0; k0 < g.top_k; k0 += kWarp) {
+      // lane k resolves slot k0 + k; rows in the borrowed tail are left to the last pass
+      const int64_t a = item * g.top_k + k0 + lane;
+      int64_t row = -1;
+      float w = 1.0f;
+      if (k0 + lane < g.top_k) {
+        const int32_t i = __ldg(g.positions + a);
+        if (i < 0 || i >= g.n || __ldg(g.indices + i) != a) {
+          flag_status(g.status, MOE_STATUS_BAD_INDEX);
+        } else {
+          row = position_row<PADDED>(g, sb, spb, i);
+          if (row >= g.row_begin) row = -1;
+        }
+        if (kWeighted && row >= 0) w = __ldg(g.weights + a);
+      }
+      const unsigned kept = __ballot_sync(kAll, row >= 0);
+      const int nk = __popc(kept);
+      const int from = lane < nk ? (int)__fns(kept, 0, lane + 1) : 0;
+      const int64_t krow = __shfl_sync(kAll, row, from);  // lane q: row of the q-th kept slot
+      const float kw = __shfl_sync(kAll, w, from);
+      for (int q0 = 0; q0 < nk; q0 += KQ) {
+        const int nq = min(KQ, nk - q0);
+        V* dst[KQ];
+        float wq[KQ];
+#pragma unroll
+        for (int q = 0; q < KQ; ++q) {
+          const int64_t r = __shfl_sync(kAll, krow, (q0 + q) & (kWarp - 1));
+          dst[q] = out + (q < nq ? r : 0) * g.vecs;
+          wq[q] = __shfl_sync(kAll, kw, (q0 + q) & (kWarp - 1));
+        }
+        for (int64_t c0 = 0; c0 < g.vecs; c0 += kWarp * U) {
+          V v[U];
+#pragma unroll
+          for (int u = 0; u < U; ++u) {
+            const int64_t c = c0 + u * kWarp + lane;
+            if (c < g.vecs) v[u] = ld_stream(src + c);
+          }
+#pragma unroll
+          for (int q = 0; q < KQ; ++q) {
+            if (q < nq) {
+#pragma unroll
+              for (int u = 0; u < U; ++u) {
+                const int64_t c = c0 + u * kWarp + lane;
+                if constexpr (kWeighted) {
+                  if (c < g.vecs) st_stream(dst[q] + c, scale_vec<ST>(v[u], wq[q]));
+                } else {
+                  if (c < g.vecs) st_stream(dst[q] + c, v[u]);
+                }
+              }
+            }
+          }
+        }
+      }
+    }
+  }
+}
+
 template <int VB, bool PADDED, typename ST>
-int launch_gather(const GatherArgs& g, cudaStream_t s) {
+int launch_gather(GatherArgs g, int64_t row_bytes, cudaStream_t s) {
   constexpr int U = VB == 32 ? 4 : (VB >= 8 ? 8 : 16);  // 128 bytes per lane in flight
-  auto k = gather_kernel<VB, U, PADDED, ST>;
-  const int64_t work_ctas = (g.rows_out + (kThreads / kWarp) - 1) / (kThreads / kWarp);
-  const int grid = persistent_grid(k, kThreads, 0, work_ctas);
-  k<<<grid, kThreads, 0, s>>>(g);
+  constexpr int kWarps = kThreads / kWarp;
+  // Borrow the last 4n bytes of the output (16-byte aligned) for the
+  // positions when the rows before them are at least some of the output.
+  const uint64_t total = (uint64_t)g.rows_out * (uint64_t)row_bytes;
+  const uint64_t need = 4ull * (uint64_t)g.n;
+  g.row_begin = 0;
+  if (g.n > 0 && total >= need + 16 + (uint64_t)row_bytes) {
+    const uintptr_t base = reinterpret_cast<uintptr_t>(g.out);
+    const uintptr_t p = (base + total - need) & ~(uintptr_t)15;
+    g.positions = reinterpret_cast<const int32_t*>(p);
+    g.row_begin = (int64_t)((p - base) / (uint64_t)row_bytes);  // rows wholly before the positions
+    const int64_t blocks = (g.n + 255) / 256;
+    positions_kernel<<<(unsigned)(blocks < 4096 ? blocks : 4096), 256, 0, s>>>(
+        g.indices, g.n, reinterpret_cast<int32_t*>(p), g.status);
+    if (check_launch() != MOE_OK) return MOE_ERR_CUDA;
+    auto kt = gather_token_kernel<VB, U, PADDED, ST>;
+    kt<<<persistent_grid(kt, kThreads, 0, (g.T + g.row_begin + kWarps - 1) / kWarps), kThreads, 0, s>>>(g);
+    if (check_launch() != MOE_OK) return MOE_ERR_CUDA;
+  }
+  auto k = gather_kernel<VB, U, PADDED, ST>;  // rows [row_begin, rows_out), destination-major
+  k<<<persistent_grid(k, kThreads, 0, (g.rows_out - g.row_begin + kWarps - 1) / kWarps), kThreads, 0, s>>>(g);
   return check_launch();
 }
 
@@ -182,13 +380,13 @@ int dispatch_vec(GatherArgs g, int elem, cudaStream_t s) {
   if (vb == 0) return MOE_ERR_UNSUPPORTED;
   g.vecs = row_bytes / vb;
   switch (vb) {
-    case 32: return launch_gather<32, PADDED, ST>(g, s);
-    case 16: return launch_gather<16, PADDED, ST>(g, s);
-    case 8: return launch_gather<8, PADDED, ST>(g, s);
-    case 4: return launch_gather<4, PADDED, ST>(g, s);
+    case 32: return launch_gather<32, PADDED, ST>(g, row_bytes, s);
+    case 16: return launch_gather<16, PADDED, ST>(g, row_bytes, s);
+    case 8: return launch_gather<8, PADDED, ST>(g, row_bytes, s);
+    case 4: return launch_gather<4, PADDED, ST>(g, row_bytes, s);
     default:
       if constexpr (std::is_same<ST, float>::value) return MOE_ERR_UNSUPPORTED;  // fp32 rows are 4-byte multiples
-      else return launch_gather<2, PADDED, ST>(g, s);
+      else return launch_gather<2, PADDED, ST>(g, row_bytes, s);
   }
 }
 
@@ -229,6 +427,7 @@ extern "C" int moe_binned_gather(const void* x, int32_t dtype, const int32_t* in
   if (out == nullptr) return MOE_ERR_INVALID_ARG;
   GatherArgs g{static_cast<const char*>(x), static_cast<char*>(out), indices, bins, nullptr, nullptr, T * top_k,
                rows, H, E, capacity, top_k, d_status};
+  g.T = T;
   return dispatch_gather<false>(g, dtype, reinterpret_cast<cudaStream_t>(stream));
 }
 
@@ -243,6 +442,7 @@ extern "C" int moe_padded_gather(const void* x, int32_t dtype, const int32_t* in
   if (out == nullptr) return MOE_ERR_INVALID_ARG;
   GatherArgs g{static_cast<const char*>(x), static_cast<char*>(out), indices, bins, padded_bins, nullptr, T * top_k,
                out_rows, H, E, 0, top_k, d_status};
+  g.T = T;
   return dispatch_gather<true>(g, dtype, reinterpret_cast<cudaStream_t>(stream));
 }
 
@@ -259,6 +459,7 @@ extern "C" int moe_binned_gather_weighted(const void* dy, int32_t dtype, const i
   if (out == nullptr) return MOE_ERR_INVALID_ARG;
   GatherArgs g{static_cast<const char*>(dy), static_cast<char*>(out), indices, bins, nullptr, weights, T * top_k,
                rows, H, E, capacity, top_k, d_status};
+  g.T = T;
   return dispatch_gather<false>(g, dtype, reinterpret_cast<cudaStream_t>(stream));
 }
 
@@ -275,5 +476,6 @@ extern "C" int moe_padded_gather_weighted(const void* dy, int32_t dtype, const i
   if (out == nullptr) return MOE_ERR_INVALID_ARG;
   GatherArgs g{static_cast<const char*>(dy), static_cast<char*>(out), indices, bins, padded_bins, weights,
                T * top_k, out_rows, H, E, 0, top_k, d_status};
+  g.T = T;
   return dispatch_gather<true>(g, dtype, reinterpret_cast<cudaStream_t>(stream));
 }

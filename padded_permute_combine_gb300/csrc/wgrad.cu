@@ -4,19 +4,22 @@
 //  "Build Triton-Ascend Padded MoE Routing": Workflow step 6, Guardrails on
 //  unique assignment ids and reductions across column tiles).
 //
-// Source-major: one warp owns one sorted position i at a time. When i is
-// kept it streams the expert row and the gradient row of token
-// indices[i] / TOP_K, and forms their dot product in fp32 with compensated
+// Two launches. The first writes the inverse permutation of `indices` into
+// the caller's wgrad buffer (it has exactly n 32-bit slots), so no workspace
+// is needed. The second gives one warp one assignment at a time in
+// assignment order, so the TOP_K assignments of a token run on neighbouring
+// warps and share the token's gradient row through L1: each gradient row
+// leaves HBM about once instead of once per kept slot, and each kept expert
+// row is read once. Each dot product is formed in fp32 with compensated
 // summation (Ogita, Rump and Oishi, "Accurate Sum and Dot Product", SIAM J.
 // Sci. Comput. 26(6), 2005, algorithm Dot2): every product and every partial
 // sum carries its exact rounding error (TwoProduct via fma, Knuth's TwoSum),
 // the errors are summed separately and added once at the end, and the warp
 // reduction combines (sum, error) pairs the same way. For bf16 rows the
 // products are exact and the running sums use packed f32x2 instructions, two
-// independent compensated sums per register. The result is as
-// accurate as a dot computed in twice the working precision and then
-// rounded, independent of H. A dropped position writes 0. Every wgrad entry
-// is written by exactly one warp because indices is a permutation.
+// independent compensated sums per register. The result is as accurate as a
+// dot computed in twice the working precision and then rounded, independent
+// of H. A dropped slot writes 0.
 #include "common.cuh"
 #include "vec_math.cuh"
 
@@ -87,49 +90,121 @@ struct Acc2x2 {
   }
 };
 
-template <int VB, int U, typename ET, bool PADDED>
+// Load of a positions entry that the same kernel later overwrites with an
+// fp32 result (no read-only path, ordered against the stores).
+__device__ __forceinline__ int32_t ld_position(const int32_t* p) {
+  int32_t v;
+  asm volatile("ld.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+// Inverse permutation of indices, written into the caller's wgrad buffer
+// (n int32 values in its n fp32 slots): positions[indices[i]] = i. The token
+// pass reads each slot once and then overwrites it with the result.
+__global__ void positions_kernel(const int32_t* __restrict__ indices, int64_t n, int32_t* positions,
+                                 int32_t* status) {
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x) {
+    const int32_t a = __ldg(indices + i);
+    if (a >= 0 && a < n) positions[a] = (int32_t)i;
+    else flag_status(status, MOE_STATUS_BAD_INDEX);
+  }
+}
+
+// Expert row of sorted position i holding expert e, or -1 when capacity
+// drops it or the routing data are inconsistent (status flagged).
+template <bool PADDED>
+__device__ __forceinline__ int64_t expert_row(const WgradArgs& g, int64_t i, int32_t e) {
+  if (e < 0 || e >= g.E) {
+    flag_status(g.status, MOE_STATUS_BAD_EXPERT);
+    return -1;
+  }
+  const int64_t start = e > 0 ? __ldg(g.bins + e - 1) : 0;
+  const int64_t j = i - start;
+  if (j < 0 || i >= __ldg(g.bins + e)) {
+    flag_status(g.status, MOE_STATUS_BAD_BINS);
+    return -1;
+  }
+  int64_t row;
+  if (!PADDED) {
+    if (j >= g.capacity) return -1;
+    row = (int64_t)e * g.capacity + j;
+  } else {
+    row = (e > 0 ? __ldg(g.padded_bins + e - 1) : 0) + j;
+  }
+  if (row < 0 || row >= g.xe_rows) {
+    flag_status(g.status, MOE_STATUS_BAD_BINS);
+    return -1;
+  }
+  return row;
+}
+
+// Row of assignment a, whose sorted position comes from the positions pass
+// and is checked against indices, so a stale entry (indices not a
+// permutation) is caught rather than followed.
+template <bool PADDED>
+__device__ __forceinline__ int64_t assignment_row(const WgradArgs& g, int64_t a) {
+  const int32_t i = ld_position(reinterpret_cast<const int32_t*>(g.wgrad) + a);
+  if (i < 0 || i >= g.n) {
+    flag_status(g.status, MOE_STATUS_BAD_INDEX);
+    return -1;
+  }
+  const int32_t back = __ldg(g.indices + i);  // both loads issued together
+  const int32_t e = __ldg(g.bin_ids + i);
+  if (back != a) {
+    flag_status(g.status, MOE_STATUS_BAD_INDEX);
+    return -1;
+  }
+  return expert_row<PADDED>(g, i, e);
+}
+
+// Row of sorted position i and its assignment a (-1 when out of range).
+template <bool PADDED>
+__device__ __forceinline__ int64_t sorted_row(const WgradArgs& g, int64_t i, int32_t& a) {
+  a = __ldg(g.indices + i);
+  const int32_t e = __ldg(g.bin_ids + i);
+  if (a < 0 || a >= g.n) {
+    flag_status(g.status, MOE_STATUS_BAD_INDEX);
+    a = -1;
+    return -1;
+  }
+  return expert_row<PADDED>(g, i, e);
+}
+
+// One warp owns one item at a time; lane 0 resolves it to an expert row and
+// an assignment and broadcasts them, and a dropped slot writes 0. Items are
+//  - BY_ASSIGNMENT: assignments in increasing id, so the TOP_K assignments
+//    of a token run on neighbouring warps of one CTA and read the token's
+//    gradient row through L1 at about the same time (each gradient row
+//    leaves HBM about once);
+//  - otherwise sorted positions in increasing order, so kept expert rows are
+//    read in address order and the positions pass is not needed; gradient
+//    rows are loaded evict-last for their later slots.
+template <int VB, int U, typename ET, bool PADDED, bool BY_ASSIGNMENT>
 __global__ void __launch_bounds__(kThreads) wgrad_kernel(WgradArgs g) {
   using L = Lanes<VB, ET>;
   using V = typename L::V;
   constexpr int NE = L::kElems;
   constexpr bool kExact = Elem<ET>::kBytes == 2;  // bf16 x bf16 fits in fp32
+  constexpr bool kPacked = kExact && NE % 2 == 0;
   const int lane = lane_id();
   const int64_t warps = (int64_t)gridDim.x * (blockDim.x / kWarp);
   const V* __restrict__ xe = reinterpret_cast<const V*>(g.xe);
   const V* __restrict__ gr = reinterpret_cast<const V*>(g.grad);
 
-  for (int64_t i = (int64_t)blockIdx.x * (blockDim.x / kWarp) + threadIdx.x / kWarp; i < g.n; i += warps) {
-    const int32_t a = __ldg(g.indices + i);
-    if (a < 0 || a >= g.n) {
-      if (lane == 0) flag_status(g.status, MOE_STATUS_BAD_INDEX);
-      continue;
+  for (int64_t item = (int64_t)blockIdx.x * (blockDim.x / kWarp) + threadIdx.x / kWarp; item < g.n;
+       item += warps) {
+    int64_t row = 0;
+    int32_t a = (int32_t)item;
+    if (lane == 0) {
+      if constexpr (BY_ASSIGNMENT) row = assignment_row<PADDED>(g, a);
+      else row = sorted_row<PADDED>(g, item, a);
+      if (row < 0 && a >= 0) g.wgrad[a] = 0.0f;
     }
-    const int32_t e = __ldg(g.bin_ids + i);
-    int64_t row = -1;
-    if (e < 0 || e >= g.E) {
-      if (lane == 0) flag_status(g.status, MOE_STATUS_BAD_EXPERT);
-    } else {
-      const int64_t start = e > 0 ? __ldg(g.bins + e - 1) : 0;
-      const int64_t j = i - start;
-      if (j < 0 || i >= __ldg(g.bins + e)) {
-        if (lane == 0) flag_status(g.status, MOE_STATUS_BAD_BINS);
-      } else if (!PADDED) {
-        if (j < g.capacity) row = (int64_t)e * g.capacity + j;
-      } else {
-        row = (e > 0 ? __ldg(g.padded_bins + e - 1) : 0) + j;
-      }
-      if (row >= g.xe_rows) {
-        if (lane == 0) flag_status(g.status, MOE_STATUS_BAD_BINS);
-        row = -1;
-      }
-    }
-    if (row < 0) {
-      if (lane == 0) g.wgrad[a] = 0.0f;
-      continue;
-    }
+    row = __shfl_sync(0xffffffffu, row, 0);
+    a = __shfl_sync(0xffffffffu, a, 0);
+    if (row < 0) continue;
     const V* xr = xe + row * g.vecs;
-    const V* gv = gr + (int64_t)(a / g.top_k) * g.vecs;
-    constexpr bool kPacked = kExact && NE % 2 == 0;
+    const V* gv = gr + (a / g.top_k) * g.vecs;
     Acc2 acc[2];
     Acc2x2 acc2[2];
     for (int64_t c0 = 0; c0 < g.vecs; c0 += kWarp * U) {
@@ -139,7 +214,7 @@ __global__ void __launch_bounds__(kThreads) wgrad_kernel(WgradArgs g) {
         const int64_t c = c0 + u * kWarp + lane;
         if (c < g.vecs) {
           vx[u] = ld_once(xr + c);  // each expert row is read once
-          vg[u] = ld_keep(gv + c);  // the token's gradient row, once per kept slot
+          vg[u] = BY_ASSIGNMENT ? ld_l1(gv + c) : ld_keep(gv + c);
         }
       }
 #pragma unroll
@@ -172,10 +247,22 @@ __global__ void __launch_bounds__(kThreads) wgrad_kernel(WgradArgs g) {
   }
 }
 
+// Padded rows hold every assignment (TOP_K per token): assignment order,
+// which reads each gradient row once, measured fastest there. Binned rows
+// hold only the slots within capacity (fewer per token, so fewer gradient
+// re-reads, which L2 catches): sorted order, with its address-ordered row
+// reads, measured fastest there.
 template <int VB, typename ET, bool PADDED>
 int launch_wgrad(const WgradArgs& g, cudaStream_t s) {
+  constexpr bool kByAssignment = PADDED;
+  if (kByAssignment) {
+    const int64_t blocks = (g.n + 255) / 256;
+    positions_kernel<<<(unsigned)(blocks < 4096 ? blocks : 4096), 256, 0, s>>>(
+        g.indices, g.n, reinterpret_cast<int32_t*>(g.wgrad), g.status);
+    if (check_launch() != MOE_OK) return MOE_ERR_CUDA;
+  }
   constexpr int U = VB == 32 ? 2 : (VB == 16 ? 4 : 8);  // 64 bytes per lane and operand in flight
-  auto k = wgrad_kernel<VB, U, ET, PADDED>;
+  auto k = wgrad_kernel<VB, U, ET, PADDED, kByAssignment>;
   const int64_t work_ctas = (g.n + (kThreads / kWarp) - 1) / (kThreads / kWarp);
   k<<<persistent_grid(k, kThreads, 0, work_ctas), kThreads, 0, s>>>(g);
   return check_launch();

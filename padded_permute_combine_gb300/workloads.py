@@ -256,14 +256,16 @@ def mixtral_8x22b_padded(seed=0) -> Routing:
                                pad_multiple=128, j=8, seed=seed)
 
 
-def deepseek_v3(seed=0, n_empty=0) -> Routing:
+def deepseek_v3(seed=0, n_empty=0, capacity_factor=1.0, pad_multiple=128) -> Routing:
     """DeepSeek-V3-shaped case: T=8192, H=7168, E=256, K=8 (65536 assignments),
-    bf16, capacity ceil(T*K/E) = 256, padding multiple 128, Zipf(1.1)
-    popularity."""
+    bf16, capacity ceil(capacity_factor*T*K/E) (256 at the default factor
+    1.0), padding multiple 128 by default, Zipf(1.1) popularity."""
     T, E, K = 8192, 256, 8
     name = "deepseek-v3-bf16" + ("-empty%d" % n_empty if n_empty else "")
-    return zipf_routing(name, T, 7168, E, K, BF16, capacity=math.ceil(T * K / E),
-                        pad_multiple=128, s=1.1, n_empty=n_empty, seed=seed)
+    if capacity_factor != 1.0 or pad_multiple != 128:
+        name += "-cf%g-m%d" % (capacity_factor, pad_multiple)
+    return zipf_routing(name, T, 7168, E, K, BF16, capacity=math.ceil(capacity_factor * T * K / E),
+                        pad_multiple=pad_multiple, s=1.1, n_empty=n_empty, seed=seed)
 
 
 def qwen2_moe_57b(seed=0) -> DenseRoutes:

@@ -166,6 +166,16 @@ def test_deepseek_v3_with_empty_experts_bf16():
     run_routing(r)
 
 
+@pytest.mark.slow
+@pytest.mark.parametrize("capacity_factor,pad_multiple", [(0.5, 16), (1.25, 64), (2.0, 256)])
+def test_deepseek_v3_capacity_factor_and_padding_multiple(capacity_factor, pad_multiple):
+    # the same DeepSeek-V3-shaped batch at other capacity factors (128, 320
+    # and 512 rows per expert) and padding multiples
+    r = wl.deepseek_v3(capacity_factor=capacity_factor, pad_multiple=pad_multiple)
+    assert r.capacity == {0.5: 128, 1.25: 320, 2.0: 512}[capacity_factor]
+    run_routing(r)
+
+
 # ------------------------------------------------------------ edge matrix
 
 @pytest.mark.parametrize("H", [1, 7, 8, 255, 1003, 7168])

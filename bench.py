@@ -267,6 +267,23 @@ class Path:
         }
 
 
+    def survey_bytes(self) -> dict:
+        """The per-kernel byte counts of the survey's measurement plan, which
+        count a token row once per kept slot in the gathers and a gradient
+        row once per kept slot in wgrad (a schedule without row reuse)."""
+        r = self.r
+        T, H, E, n, b = r.T, r.H, r.E, self.n, 2
+        kept, P, cap = self.kept, self.P, r.capacity
+        return {
+            "binned_gather": kept * H * b + E * cap * H * b + 8 * n + 4 * E,
+            "padded_gather": n * H * b + P * H * b + 8 * n + 8 * E,
+            "binned_scatter": kept * H * b + T * H * b + 16 * n + 4 * E,
+            "padded_scatter": n * H * b + T * H * b + 16 * n + 8 * E,
+            "binned_wgrad": 2 * kept * H * b + 12 * n + 4 * E,
+            "padded_wgrad": 2 * n * H * b + 12 * n + 8 * E,
+        }
+
+
 class ClockSampler:
     """nvidia-smi clocks and throttle reasons while the timed region runs."""
 
@@ -384,12 +401,16 @@ def run_gpu(args, rank, world, local_rank):
     value = weak_scaling_value(world, n, args.steps, total_ms)
     peak, peak_kind = measured_peak()
     algo = path.algorithmic_bytes()
+    survey = path.survey_bytes()
     kern = {}
     for name, launches, _ in ops:
         ms = statistics.mean(per_kernel[name])
         gbs = algo[name] / (ms * 1e-3) / 1e9
         kern[name] = {"ms": round(ms, 5), "algorithmic_bytes": algo[name], "gbs": round(gbs, 1),
                       "frac_of_%s_peak" % peak_kind: round(gbs / peak, 4), "launches": launches}
+        if name in survey:
+            kern[name]["survey_bytes"] = survey[name]
+            kern[name]["survey_gbs"] = round(survey[name] / (ms * 1e-3) / 1e9, 1)
     hot = ["binned_gather", "binned_scatter", "binned_wgrad", "padded_gather", "padded_scatter", "padded_wgrad"]
     hot_bytes = sum(algo[k] for k in hot)
     hot_ms = sum(kern[k]["ms"] for k in hot)

@@ -223,8 +223,10 @@ class Path:
     def next_ops(self):
         """(name, callable, algorithmic bytes) of the rows beyond the routing
         path that are built: router top-k gating (sigmoid, renormalised, on
-        N(0,1) logits [T, E]) and the weighted gathers, i.e. the combine's
-        gradient with respect to the expert rows, with grad as dy."""
+        N(0,1) logits [T, E]), the weighted gathers, i.e. the combine's
+        gradient with respect to the expert rows, with grad as dy, and route
+        build + gather in one call (to compare with the step's route_build
+        plus binned / padded gather)."""
         p, r, rt = self.p, self.r, self.route
         T, H, E, K, n, b = r.T, r.H, r.E, r.K, self.n, 2
         w = self.pi.view(-1)
@@ -234,6 +236,8 @@ class Path:
             self.logits = self.torch.from_numpy(wl.normal((T, E), wl.F32, r.seed, 11)).to(self.dev)
             self.g_out = (self.torch.empty((T, K), dtype=self.torch.int32, device=self.dev),
                           self.torch.empty((T, K), dtype=self.torch.float32, device=self.dev))
+            self.froute = p.Route(*(self.torch.empty_like(t) for t in rt))
+        algo = self.algorithmic_bytes()
         return [
             ("topk_gating", lambda: p.moe_topk_gating(self.logits, K, "sigmoid", True, out=self.g_out),
              T * E * 4 + T * K * 8),
@@ -244,6 +248,14 @@ class Path:
              lambda: p.moe_padded_gather_weighted(self.grad, rt.indices, rt.bins, rt.padded_bins, w, K,
                                                   out_rows=self.P, out=self.gwp),
              T * H * b + self.P * H * b + 8 * n + 8 * E),
+            ("route_build_binned_gather",
+             lambda: p.moe_route_build_binned_gather(self.idx, self.x, E, r.capacity, r.pad_multiple,
+                                                     route=self.froute, out=self.gwb, workspace=self.ws),
+             algo["route_build"] + algo["binned_gather"]),
+            ("route_build_padded_gather",
+             lambda: p.moe_route_build_padded_gather(self.idx, self.x, E, r.pad_multiple, out_rows=self.P,
+                                                     route=self.froute, out=self.gwp, workspace=self.ws),
+             algo["route_build"] + algo["padded_gather"]),
         ]
 
     def algorithmic_bytes(self) -> dict:

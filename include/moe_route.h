@@ -68,7 +68,8 @@ enum moe_device_status {
   MOE_STATUS_BAD_EXPERT = 1,   /* expert id outside [0, E) */
   MOE_STATUS_BAD_INDEX = 2,    /* an index or position outside its range */
   MOE_STATUS_BAD_BINS = 4,     /* bins / padded_bins not monotonic or not consistent */
-  MOE_STATUS_ROWS_MISMATCH = 8 /* padded_bins[E-1] exceeds the rows the caller provided */
+  MOE_STATUS_ROWS_MISMATCH = 8, /* padded_bins[E-1] exceeds the rows the caller provided */
+  MOE_STATUS_TIMEOUT = 16       /* a bounded wait on an asynchronous copy gave up; outputs unspecified */
 };
 
 /* Library limits (inclusive). */
@@ -210,6 +211,44 @@ int moe_padded_gather_weighted(const void* dy, int32_t dtype,
                                int32_t num_experts, int32_t top_k, void* out,
                                int64_t out_rows, int32_t* d_status,
                                moe_stream_t stream);
+
+/*
+ * Route build and gather in one call ([padded] Workflow steps 1-5;
+ * [binned] Workflow steps 1-3): exactly moe_route_build of
+ * top_expert [n = T*top_k] (all five outputs, positions required) followed
+ * by moe_binned_gather / moe_padded_gather of x, with the same results. The
+ * gather reads the positions the route build has just written, so it needs
+ * neither its inverse-permutation pass nor the borrowed output tail: four
+ * launches instead of six, and x is read once per token.
+ *   workspace: >= moe_route_build_workspace_size(n, E) bytes.
+ *   padded: out has out_rows rows; the caller does not know
+ *   padded_bins[E-1] before the call, so out_rows is a bound, such as
+ *   n + E*(pad_multiple-1) (every padded total is at most that); rows at
+ *   or beyond padded_bins[E-1] are zero-filled, and MOE_STATUS_ROWS_MISMATCH
+ *   is set if padded_bins[E-1] exceeds out_rows.
+ * Errors as for the two calls; argument errors return before anything is
+ * enqueued.
+ */
+int moe_route_build_binned_gather(const int32_t* top_expert, const void* x,
+                                  int32_t dtype, int64_t num_tokens,
+                                  int64_t hidden, int32_t num_experts,
+                                  int32_t top_k, int32_t capacity,
+                                  int32_t pad_multiple, int32_t* indices,
+                                  int32_t* bin_ids, int32_t* bins,
+                                  int32_t* padded_bins, int32_t* positions,
+                                  void* out, void* workspace,
+                                  size_t workspace_bytes, int32_t* d_status,
+                                  moe_stream_t stream);
+int moe_route_build_padded_gather(const int32_t* top_expert, const void* x,
+                                  int32_t dtype, int64_t num_tokens,
+                                  int64_t hidden, int32_t num_experts,
+                                  int32_t top_k, int32_t pad_multiple,
+                                  int32_t* indices, int32_t* bin_ids,
+                                  int32_t* bins, int32_t* padded_bins,
+                                  int32_t* positions, void* out,
+                                  int64_t out_rows, void* workspace,
+                                  size_t workspace_bytes, int32_t* d_status,
+                                  moe_stream_t stream);
 
 /*
  * Scatter / combine ([binned] Workflow step 5, Guardrails; [padded]

@@ -14,6 +14,8 @@ from .ops import (  # noqa: F401
     moe_padded_scatter,
     moe_padded_wgrad,
     moe_route_build,
+    moe_route_build_binned_gather,
+    moe_route_build_padded_gather,
     moe_routing_map_to_indices_bwd,
     moe_routing_map_to_indices_fwd,
     moe_topk_gating,

@@ -17,6 +17,7 @@ HEADER = os.path.join(os.path.dirname(PKG), "include", "moe_route.h")
 MOE_OK, MOE_ERR_INVALID_ARG, MOE_ERR_UNSUPPORTED, MOE_ERR_CUDA = 0, 1, 2, 3
 MOE_F32, MOE_BF16 = 0, 1
 MOE_STATUS_BAD_EXPERT, MOE_STATUS_BAD_INDEX, MOE_STATUS_BAD_BINS, MOE_STATUS_ROWS_MISMATCH = 1, 2, 4, 8
+MOE_STATUS_TIMEOUT = 16
 MOE_MAX_EXPERTS, MOE_MAX_TOP_K = 4096, 64
 MOE_GATING_SOFTMAX, MOE_GATING_SIGMOID = 0, 1
 MOE_GATING_MAX_EXPERTS = 1024
@@ -38,6 +39,10 @@ SIGNATURES = {
     "moe_binned_gather_weighted": (ctypes.c_int, [_P, _I32, _P, _P, _P, _I64, _I64, _I32, _I32, _I32, _P, _P, _P]),
     "moe_padded_gather_weighted": (ctypes.c_int, [_P, _I32, _P, _P, _P, _P, _I64, _I64, _I32, _I32, _P, _I64, _P,
                                                   _P]),
+    "moe_route_build_binned_gather": (ctypes.c_int, [_P, _P, _I32, _I64, _I64, _I32, _I32, _I32, _I32, _P, _P, _P,
+                                                     _P, _P, _P, _P, _SZ, _P, _P]),
+    "moe_route_build_padded_gather": (ctypes.c_int, [_P, _P, _I32, _I64, _I64, _I32, _I32, _I32, _P, _P, _P, _P,
+                                                     _P, _P, _I64, _P, _SZ, _P, _P]),
     "moe_scatter_workspace_size": (_SZ, [_I64]),
     "moe_binned_scatter": (ctypes.c_int, [_P, _I32, _P, _P, _P, _P, _P, _I64, _I64, _I32, _I32, _I32, _P, _P, _SZ,
                                           _P, _P]),

@@ -269,6 +269,7 @@ __global__ void __launch_bounds__(kThreads) gather_token_kernel(GatherArgs g) {
       if (PADDED) ok = ok && (int64_t)spb[e] - (e > 0 ? spb[e - 1] : 0) >= (int64_t)sb[e] - prev;
       if (!ok) flag_status(g.status, MOE_STATUS_BAD_BINS);
     }
+    if (PADDED && threadIdx.x == 0 && spb[g.E - 1] > g.rows_out) flag_status(g.status, MOE_STATUS_ROWS_MISMATCH);
   }
 
   const int lane = lane_id();
@@ -345,12 +346,203 @@ __global__ void __launch_bounds__(kThreads) gather_token_kernel(GatherArgs g) {
   }
 }
 
+// ------------------------------------------------- bulk-copy token pass (TMA)
+//
+// The plain gather's token pass with the Tensor Memory Accelerator doing
+// the copies: per row chunk, lane 0 of a warp issues one bulk load of the
+// token row chunk into shared memory (completion tracked by an mbarrier)
+// and one bulk store of it to each kept output row; zero rows are bulk
+// stores of a zeroed chunk. One instruction moves up to kTmaChunk bytes, so
+// the load/store units are no longer the limit (the register path issues
+// one 32-byte store per lane per vector and stalls on their queue). Each
+// warp alternates two chunk buffers, so a chunk's load overlaps the
+// previous chunk's stores. Every mbarrier wait is bounded: after kSpinLimit
+// polls the warp sets MOE_STATUS_TIMEOUT, drains its stores and stops.
+
+#ifndef MOE_GATHER_TMA
+#define MOE_GATHER_TMA 1
+#endif
+constexpr int kTmaWarps = 4;
+constexpr int kTmaThreads = kTmaWarps * kWarp;
+constexpr int kTmaChunk = 8192;  // bytes per staged row chunk
+constexpr size_t kTmaSmem = (size_t)kTmaChunk * (1 + 2 * kTmaWarps) + 16 * kTmaWarps;
+constexpr int kSpinLimit = 1 << 22;
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
+
+__device__ __forceinline__ void mbar_init(uint32_t bar) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(bar) : "memory");
+}
+
+// Expect `bytes` on the barrier, then copy global -> shared; completion
+// arrives on the barrier.
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+               "l"(src), "r"(bytes), "r"(bar)
+               : "memory");
+}
+
+// Polls the barrier's phase with the given parity at most kSpinLimit times.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
+  for (int it = 0; it < kSpinLimit; ++it) {
+    uint32_t done;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}"
+        : "=r"(done)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    if (done) return true;
+  }
+  return false;
+}
+
+__device__ __forceinline__ void bulk_store(void* dst, uint32_t src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(dst), "r"(src), "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+// Waits until at most one committed group still reads shared memory.
+__device__ __forceinline__ void bulk_wait_read_but_one() {
+  asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
+}
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+__device__ __forceinline__ void fence_async_shared() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+
+template <bool PADDED>
+__global__ void __launch_bounds__(kTmaThreads) gather_tma_kernel(GatherArgs g, int64_t row_bytes) {
+  constexpr unsigned kAll = 0xffffffffu;
+  extern __shared__ __align__(128) unsigned char tsm[];
+  __shared__ int32_t sbins[kStageMax];
+  __shared__ int32_t spbins[PADDED ? kStageMax : 1];
+  const int warp = threadIdx.x / kWarp, lane = lane_id();
+  unsigned char* zero = tsm;
+  unsigned char* bufs = tsm + (size_t)kTmaChunk * (1 + 2 * warp);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(tsm + (size_t)kTmaChunk * (1 + 2 * kTmaWarps)) + 2 * warp;
+  for (int q = threadIdx.x; q < kTmaChunk / 16; q += blockDim.x) reinterpret_cast<uint4*>(zero)[q] = make_uint4(0, 0, 0, 0);
+  if (lane == 0) {
+    mbar_init(smem_u32(bars));
+    mbar_init(smem_u32(bars + 1));
+  }
+  const bool staged = g.E <= kStageMax;
+  if (staged) {
+    for (int e = threadIdx.x; e < g.E; e += blockDim.x) {
+      sbins[e] = __ldg(g.bins + e);
+      if (PADDED) spbins[e] = __ldg(g.padded_bins + e);
+    }
+  }
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  fence_async_shared();  // the zero chunk and the barriers, for the bulk-copy unit
+  __syncthreads();
+  const int32_t* sb = staged ? sbins : g.bins;
+  const int32_t* spb = PADDED ? (staged ? spbins : g.padded_bins) : nullptr;
+  if (blockIdx.x == 0) {
+    for (int e = threadIdx.x; e < g.E; e += blockDim.x) {
+      const int32_t prev = e > 0 ? sb[e - 1] : 0;
+      bool ok = sb[e] >= prev && (e < g.E - 1 || sb[e] <= g.n);
+      if (PADDED) ok = ok && (int64_t)spb[e] - (e > 0 ? spb[e - 1] : 0) >= (int64_t)sb[e] - prev;
+      if (!ok) flag_status(g.status, MOE_STATUS_BAD_BINS);
+    }
+    if (PADDED && threadIdx.x == 0 && spb[g.E - 1] > g.rows_out) flag_status(g.status, MOE_STATUS_ROWS_MISMATCH);
+  }
+
+  const int64_t warps = (int64_t)gridDim.x * kTmaWarps;
+  const int64_t items = g.T + g.row_begin;  // tokens, then the rows this kernel may zero-fill
+  uint32_t parity = 0;                       // bit b: parity of buffer b's next completion
+  int use = 0;                               // buffer of the next chunk
+  bool ok = true;
+  for (int64_t item = (int64_t)blockIdx.x * kTmaWarps + warp; item < items && ok; item += warps) {
+    if (item >= g.T) {
+      const int64_t r = item - g.T;
+      if (lane == 0 && is_zero_row<PADDED>(g, sb, spb, r)) {
+        for (int64_t off = 0; off < row_bytes; off += kTmaChunk)
+          bulk_store(g.out + r * row_bytes + off, smem_u32(zero), (uint32_t)min((int64_t)kTmaChunk, row_bytes - off));
+        bulk_commit();
+      }
+      continue;
+    }
+    for (int k0 = 0; k0 < g.top_k && ok; k0 += kWarp) {
+      const int64_t a = item * g.top_k + k0 + lane;
+      int64_t row = -1;
+      if (k0 + lane < g.top_k) {
+        const int32_t i = __ldg(g.positions + a);
+        if (i < 0 || i >= g.n || __ldg(g.indices + i) != a) {
+          flag_status(g.status, MOE_STATUS_BAD_INDEX);
+        } else {
+          row = position_row<PADDED>(g, sb, spb, i);
+          if (row >= g.row_begin) row = -1;
+        }
+      }
+      const unsigned kept = __ballot_sync(kAll, row >= 0);
+      const int nk = __popc(kept);
+      if (nk == 0) continue;
+      const int from = lane < nk ? (int)__fns(kept, 0, lane + 1) : 0;
+      const int64_t krow = __shfl_sync(kAll, row, from);  // lane q: row of the q-th kept slot
+      for (int64_t off = 0; off < row_bytes; off += kTmaChunk) {
+        const uint32_t bytes = (uint32_t)min((int64_t)kTmaChunk, row_bytes - off);
+        const uint32_t buf = smem_u32(bufs + (size_t)use * kTmaChunk);
+        const uint32_t bar = smem_u32(bars + use);
+        bool got = true;
+        if (lane == 0) {
+          bulk_wait_read_but_one();  // the stores that last read this buffer have finished
+          bulk_load(buf, g.x + item * row_bytes + off, bytes, bar);
+          got = mbar_wait(bar, (parity >> use) & 1u);
+          parity ^= 1u << use;
+        }
+        ok = __shfl_sync(kAll, (int)got, 0) != 0;
+        if (!ok) break;
+        for (int q = 0; q < nk; ++q) {
+          const int64_t r = __shfl_sync(kAll, krow, q);
+          if (lane == 0) bulk_store(g.out + r * row_bytes + off, buf, bytes);
+        }
+        if (lane == 0) bulk_commit();
+        use ^= 1;
+      }
+    }
+  }
+  if (lane == 0) {
+    if (!ok) flag_status(g.status, MOE_STATUS_TIMEOUT);
+    bulk_wait_all();  // the stores have read shared memory and written the output
+  }
+}
+
+// Launches the bulk-copy token pass; false when the rows or pointers do not
+// meet the 16-byte rule of the bulk copies (the register path runs instead).
+template <bool PADDED>
+bool launch_gather_tma(const GatherArgs& g, int64_t row_bytes, cudaStream_t s, int* rc) {
+  if (!MOE_GATHER_TMA || row_bytes % 16 != 0 || !aligned(g.x, 16) || !aligned(g.out, 16)) return false;
+  auto k = gather_tma_kernel<PADDED>;
+  static int configured[64] = {0};
+  int dev = 0;
+  (void)cudaGetDevice(&dev);
+  if (dev < 0 || dev >= 64 || !configured[dev]) {
+    if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kTmaSmem) != cudaSuccess) {
+      (void)cudaGetLastError();
+      return false;
+    }
+    if (dev >= 0 && dev < 64) configured[dev] = 1;
+  }
+  const int64_t work_ctas = (g.T + g.row_begin + kTmaWarps - 1) / kTmaWarps;
+  k<<<persistent_grid(k, kTmaThreads, kTmaSmem, work_ctas), kTmaThreads, kTmaSmem, s>>>(g, row_bytes);
+  *rc = check_launch();
+  return true;
+}
+
 template <int VB, bool PADDED, typename ST>
 int launch_gather(GatherArgs g, int64_t row_bytes, cudaStream_t s) {
   constexpr int U = VB == 32 ? 4 : (VB >= 8 ? 8 : 16);  // 128 bytes per lane in flight
   constexpr int kWarps = kThreads / kWarp;
   // Borrow the last 4n bytes of the output (16-byte aligned) for the
   // positions when the rows before them are at least some of the output.
+  if (g.positions != nullptr) {
+    // The caller's positions (route build in the same call): one token pass over every row.
+    g.row_begin = g.rows_out;
+    int rc = MOE_OK;
+    if (std::is_void<ST>::value && launch_gather_tma<PADDED>(g, row_bytes, s, &rc)) return rc;
+    auto kt = gather_token_kernel<VB, U, PADDED, ST>;
+    kt<<<persistent_grid(kt, kThreads, 0, (g.T + g.row_begin + kWarps - 1) / kWarps), kThreads, 0, s>>>(g);
+    return check_launch();
+  }
   const uint64_t total = (uint64_t)g.rows_out * (uint64_t)row_bytes;
   const uint64_t need = 4ull * (uint64_t)g.n;
   g.row_begin = 0;
@@ -363,9 +555,13 @@ int launch_gather(GatherArgs g, int64_t row_bytes, cudaStream_t s) {
     positions_kernel<<<(unsigned)(blocks < 4096 ? blocks : 4096), 256, 0, s>>>(
         g.indices, g.n, reinterpret_cast<int32_t*>(p), g.status);
     if (check_launch() != MOE_OK) return MOE_ERR_CUDA;
-    auto kt = gather_token_kernel<VB, U, PADDED, ST>;
-    kt<<<persistent_grid(kt, kThreads, 0, (g.T + g.row_begin + kWarps - 1) / kWarps), kThreads, 0, s>>>(g);
-    if (check_launch() != MOE_OK) return MOE_ERR_CUDA;
+    int rc = MOE_OK;
+    if (!(std::is_void<ST>::value && launch_gather_tma<PADDED>(g, row_bytes, s, &rc))) {
+      auto kt = gather_token_kernel<VB, U, PADDED, ST>;
+      kt<<<persistent_grid(kt, kThreads, 0, (g.T + g.row_begin + kWarps - 1) / kWarps), kThreads, 0, s>>>(g);
+      rc = check_launch();
+    }
+    if (rc != MOE_OK) return MOE_ERR_CUDA;
   }
   auto k = gather_kernel<VB, U, PADDED, ST>;  // rows [row_begin, rows_out), destination-major
   k<<<persistent_grid(k, kThreads, 0, (g.rows_out - g.row_begin + kWarps - 1) / kWarps), kThreads, 0, s>>>(g);
@@ -478,4 +674,52 @@ extern "C" int moe_padded_gather_weighted(const void* dy, int32_t dtype, const i
                T * top_k, out_rows, H, E, 0, top_k, d_status};
   g.T = T;
   return dispatch_gather<true>(g, dtype, reinterpret_cast<cudaStream_t>(stream));
+}
+
+// Route build and gather in one call: the gather consumes the positions the
+// route build writes, so it needs neither the inverse-permutation pass nor
+// the borrowed output tail (route build's three launches + one token pass).
+static int route_then_gather(const int32_t* top_expert, int32_t E, int32_t pad_multiple, int32_t* indices,
+                             int32_t* bin_ids, int32_t* bins, int32_t* padded_bins, int32_t* positions,
+                             void* workspace, size_t workspace_bytes, GatherArgs g, int32_t dtype, bool padded,
+                             cudaStream_t s) {
+  if (positions == nullptr || (padded && padded_bins == nullptr)) return MOE_ERR_INVALID_ARG;
+  if (g.out == nullptr && g.rows_out > 0 && g.vecs > 0) return MOE_ERR_INVALID_ARG;
+  const int rc = moe_route_build(top_expert, g.n, E, pad_multiple, indices, bin_ids, bins, padded_bins, positions,
+                                 workspace, workspace_bytes, g.status, reinterpret_cast<moe_stream_t>(s));
+  if (rc != MOE_OK || g.rows_out == 0 || g.vecs == 0) return rc;
+  g.positions = positions;
+  return padded ? dispatch_gather<true>(g, dtype, s) : dispatch_gather<false>(g, dtype, s);
+}
+
+extern "C" int moe_route_build_binned_gather(const int32_t* top_expert, const void* x, int32_t dtype, int64_t T,
+                                             int64_t H, int32_t E, int32_t top_k, int32_t capacity,
+                                             int32_t pad_multiple, int32_t* indices, int32_t* bin_ids,
+                                             int32_t* bins, int32_t* padded_bins, int32_t* positions, void* out,
+                                             void* workspace, size_t workspace_bytes, int32_t* d_status,
+                                             moe_stream_t stream) {
+  const int rc = gather_checks(x, dtype, indices, bins, T, H, E, top_k, out, d_status);
+  if (rc != MOE_OK) return rc;
+  if (capacity < 0) return MOE_ERR_INVALID_ARG;
+  GatherArgs g{static_cast<const char*>(x), static_cast<char*>(out), indices, bins, nullptr, nullptr, T * top_k,
+               (int64_t)E * capacity, H, E, capacity, top_k, d_status};
+  g.T = T;
+  return route_then_gather(top_expert, E, pad_multiple, indices, bin_ids, bins, padded_bins, positions, workspace,
+                           workspace_bytes, g, dtype, false, reinterpret_cast<cudaStream_t>(stream));
+}
+
+extern "C" int moe_route_build_padded_gather(const int32_t* top_expert, const void* x, int32_t dtype, int64_t T,
+                                             int64_t H, int32_t E, int32_t top_k, int32_t pad_multiple,
+                                             int32_t* indices, int32_t* bin_ids, int32_t* bins,
+                                             int32_t* padded_bins, int32_t* positions, void* out, int64_t out_rows,
+                                             void* workspace, size_t workspace_bytes, int32_t* d_status,
+                                             moe_stream_t stream) {
+  const int rc = gather_checks(x, dtype, indices, bins, T, H, E, top_k, out, d_status);
+  if (rc != MOE_OK) return rc;
+  if (out_rows < 0) return MOE_ERR_INVALID_ARG;
+  GatherArgs g{static_cast<const char*>(x), static_cast<char*>(out), indices, bins, padded_bins, nullptr,
+               T * top_k, out_rows, H, E, 0, top_k, d_status};
+  g.T = T;
+  return route_then_gather(top_expert, E, pad_multiple, indices, bin_ids, bins, padded_bins, positions, workspace,
+                           workspace_bytes, g, dtype, true, reinterpret_cast<cudaStream_t>(stream));
 }

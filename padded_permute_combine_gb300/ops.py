@@ -157,6 +157,68 @@ def moe_padded_gather_weighted(dy: torch.Tensor, indices: torch.Tensor, bins: to
     return out
 
 
+def _new_route(n: int, num_experts: int, dev) -> Route:
+    return Route(*(torch.empty(n, dtype=torch.int32, device=dev) for _ in range(2)),
+                 torch.empty(num_experts, dtype=torch.int32, device=dev),
+                 torch.empty(num_experts, dtype=torch.int32, device=dev),
+                 torch.empty(n, dtype=torch.int32, device=dev))
+
+
+def moe_route_build_binned_gather(top_expert: torch.Tensor, x: torch.Tensor, num_experts: int, capacity: int,
+                                  pad_multiple: int = 1, route: Route | None = None, out: torch.Tensor | None = None,
+                                  workspace: torch.Tensor | None = None,
+                                  status: torch.Tensor | None = None) -> tuple[Route, torch.Tensor]:
+    """Route build of top_expert [T, K] and binned gather of x [T, H] in one
+    call: (route, [E, capacity, H])."""
+    te = _need(top_expert, torch.int32, "top_expert")
+    _need(x, None, "x", te.device)
+    dt = _act_dtype(x, "x")
+    T, H = x.shape
+    n = te.numel()
+    if T == 0 or n % T:
+        raise ValueError("top_expert must hold top_k choices per token of x")
+    top_k = n // T
+    if route is None:
+        route = _new_route(n, num_experts, te.device)
+    if out is None:
+        out = torch.empty((num_experts, capacity, H), dtype=x.dtype, device=x.device)
+    _need(out, x.dtype, "out", x.device)
+    ws = workspace if workspace is not None else route_workspace(n, num_experts, te.device)
+    _lib.call("moe_route_build_binned_gather", _ptr(te), _ptr(x), dt, T, H, num_experts, top_k, capacity,
+              pad_multiple, _ptr(route.indices), _ptr(route.bin_ids), _ptr(route.bins), _ptr(route.padded_bins),
+              _ptr(route.positions), _ptr(out), _ptr(ws), ws.numel() * 4, _ptr(status), _stream(x))
+    return route, out
+
+
+def moe_route_build_padded_gather(top_expert: torch.Tensor, x: torch.Tensor, num_experts: int, pad_multiple: int,
+                                  out_rows: int | None = None, route: Route | None = None,
+                                  out: torch.Tensor | None = None, workspace: torch.Tensor | None = None,
+                                  status: torch.Tensor | None = None) -> tuple[Route, torch.Tensor]:
+    """Route build of top_expert [T, K] and padded gather of x [T, H] in one
+    call: (route, [out_rows, H]). ``out_rows`` defaults to the bound
+    n + E*(pad_multiple-1); rows past padded_bins[-1] are zero."""
+    te = _need(top_expert, torch.int32, "top_expert")
+    _need(x, None, "x", te.device)
+    dt = _act_dtype(x, "x")
+    T, H = x.shape
+    n = te.numel()
+    if T == 0 or n % T:
+        raise ValueError("top_expert must hold top_k choices per token of x")
+    top_k = n // T
+    if out_rows is None:
+        out_rows = out.shape[0] if out is not None else n + num_experts * (pad_multiple - 1)
+    if route is None:
+        route = _new_route(n, num_experts, te.device)
+    if out is None:
+        out = torch.empty((out_rows, H), dtype=x.dtype, device=x.device)
+    _need(out, x.dtype, "out", x.device)
+    ws = workspace if workspace is not None else route_workspace(n, num_experts, te.device)
+    _lib.call("moe_route_build_padded_gather", _ptr(te), _ptr(x), dt, T, H, num_experts, top_k, pad_multiple,
+              _ptr(route.indices), _ptr(route.bin_ids), _ptr(route.bins), _ptr(route.padded_bins),
+              _ptr(route.positions), _ptr(out), out_rows, _ptr(ws), ws.numel() * 4, _ptr(status), _stream(x))
+    return route, out
+
+
 def scatter_workspace(n: int, device) -> torch.Tensor:
     size = _lib.load().moe_scatter_workspace_size(n)
     return torch.empty(max(1, (size + 3) // 4), dtype=torch.int32, device=device)

@@ -18,7 +18,7 @@ def lib():
 
 def test_header_and_exports_agree(lib):
     declared = _lib.header_functions()
-    assert len(declared) == len(set(declared)) == 17
+    assert len(declared) == len(set(declared)) == 19
     out = subprocess.run(["nm", "-D", "--defined-only", _lib.LIB_PATH], capture_output=True, text=True,
                          check=True).stdout
     exported = {ln.split()[-1] for ln in out.splitlines() if " T " in ln}
@@ -78,6 +78,21 @@ def test_host_validation_rejects_bad_arguments(lib):
     assert lib.moe_binned_gather_weighted(FAKE, 1, FAKE, FAKE, FAKE + 2, 4, 8, 2, 2, 1, FAKE, None, None) == 2
     assert lib.moe_padded_gather_weighted(FAKE, 0, FAKE, FAKE, None, FAKE, 4, 8, 2, 1, FAKE, 8, None, None) == 1
     assert lib.moe_padded_gather_weighted(FAKE, 0, FAKE, FAKE, FAKE, None, 4, 8, 2, 1, FAKE, 8, None, None) == 1
+    # route build + gather in one call: positions required, padded_bins required for the padded layout,
+    # bad dtype, workspace too small, negative out_rows (all before anything is enqueued)
+    ws2 = lib.moe_route_build_workspace_size(8, 2)
+    assert lib.moe_route_build_binned_gather(FAKE, FAKE, 0, 4, 8, 2, 2, 2, 1, FAKE, FAKE, FAKE, None, None, FAKE,
+                                             FAKE, ws2, None, None) == 1
+    assert lib.moe_route_build_binned_gather(FAKE, FAKE, 9, 4, 8, 2, 2, 2, 1, FAKE, FAKE, FAKE, None, FAKE, FAKE,
+                                             FAKE, ws2, None, None) == 2
+    assert lib.moe_route_build_binned_gather(FAKE, FAKE, 0, 4, 8, 2, 2, 2, 1, FAKE, FAKE, FAKE, None, FAKE, FAKE,
+                                             FAKE, 0, None, None) == 1
+    assert lib.moe_route_build_binned_gather(FAKE, FAKE, 0, 4, 8, 2, 2, -1, 1, FAKE, FAKE, FAKE, None, FAKE, FAKE,
+                                             FAKE, ws2, None, None) == 1
+    assert lib.moe_route_build_padded_gather(FAKE, FAKE, 1, 4, 8, 2, 2, 4, FAKE, FAKE, FAKE, None, FAKE, FAKE, 16,
+                                             FAKE, ws2, None, None) == 1
+    assert lib.moe_route_build_padded_gather(FAKE, FAKE, 1, 4, 8, 2, 2, 4, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, -1,
+                                             FAKE, ws2, None, None) == 1
     # gating: top_k above E, bad mode, E above the gating limit
     assert lib.moe_topk_gating(FAKE, 4, 8, 9, 0, 1, FAKE, FAKE, None) == 1
     assert lib.moe_topk_gating(FAKE, 4, 8, 2, 5, 1, FAKE, FAKE, None) == 1

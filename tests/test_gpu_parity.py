@@ -176,6 +176,53 @@ def test_deepseek_v3_capacity_factor_and_padding_multiple(capacity_factor, pad_m
     run_routing(r)
 
 
+# ------------------------------------------------------------ route build + gather in one call
+
+def run_fused(r: wl.Routing, binned=True, padded=True):
+    """The one-call route build + gather against the oracle's route build and
+    gathers: all five route outputs and the gathered tensor, bit for bit."""
+    E, m = r.E, r.pad_multiple or 1
+    te, x = to_dev(r.top_expert, DEV), to_dev(r.x, DEV)
+    o = oracle.route_build(r.top_expert, E, m)
+    st = status_word()
+    if binned:
+        route, xb = p.moe_route_build_binned_gather(te, x, E, r.capacity, m, status=st)
+        for k in ("indices", "bin_ids", "bins", "padded_bins", "positions"):
+            assert_bits_equal(to_host(getattr(route, k)), o[k], "%s fused binned route.%s" % (r.name, k))
+        o_xb = oracle.binned_gather(r.x, o["indices"], o["bin_ids"], o["bins"], E, r.capacity, r.K)
+        assert_bits_equal(to_host(xb), o_xb, r.name + " fused binned_gather")
+    if padded:
+        route, xp = p.moe_route_build_padded_gather(te, x, E, m, status=st)  # out_rows: the bound n + E*(m-1)
+        for k in ("indices", "bin_ids", "bins", "padded_bins", "positions"):
+            assert_bits_equal(to_host(getattr(route, k)), o[k], "%s fused padded route.%s" % (r.name, k))
+        P = int(o["padded_bins"][-1])
+        assert xp.shape[0] == r.n + E * (m - 1) >= P
+        o_xp = oracle.padded_gather(r.x, o["indices"], o["bin_ids"], o["bins"], o["padded_bins"], r.K)
+        got = to_host(xp)
+        assert_bits_equal(got[:P], o_xp, r.name + " fused padded_gather")
+        assert not got[P:].any(), r.name + " fused padded_gather rows past padded_bins[-1] not zero"
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0, "device status %d on valid input" % int(st.item())
+
+
+def test_fused_route_gather_tiny_and_edges():
+    run_fused(wl.pr1())
+    run_fused(wl.uniform_routing("fused-k33", 29, 24, 48, 33, wl.BF16, capacity=5, pad_multiple=8, seed=33))
+    run_fused(wl.uniform_routing("fused-h7", 37, 7, 6, 2, wl.BF16, capacity=9, pad_multiple=4, seed=7))
+    run_fused(wl.uniform_routing("fused-t1", 1, 40, 4, 2, wl.F32, capacity=1, pad_multiple=2, seed=7))
+    r = wl.zipf_routing("fused-cap0", 300, 40, 16, 4, wl.F32, pad_multiple=3, seed=5)
+    r.capacity = 0
+    run_fused(r, padded=False)
+    r = wl.uniform_routing("fused-even", 64, 16, 8, 2, wl.BF16, capacity=12, pad_multiple=8, distinct=False, seed=2)
+    r.top_expert = (r.top_expert // 2 * 2).astype(np.int32)  # odd experts empty
+    run_fused(r)
+
+
+@pytest.mark.slow
+def test_fused_route_gather_deepseek_v3():
+    run_fused(wl.deepseek_v3())
+
+
 # ------------------------------------------------------------ edge matrix
 
 @pytest.mark.parametrize("H", [1, 7, 8, 255, 1003, 7168])

@@ -49,6 +49,8 @@ struct GatherArgs {
   int64_t T = 0;
   int64_t row_begin = 0;              // first row the destination-major kernel writes
   const int32_t* positions = nullptr;  // token-major path: inverse of indices, in the tail of out
+  int64_t segs = 1;      // token-major path: work items per token (column segments of its row)
+  int64_t seg_len = 0;   // vectors (register pass) or bytes (bulk-copy pass) per segment
 };
 
 // Assignment id whose token fills output row `row`, or -1 for a zero row.
@@ -243,8 +245,12 @@ __device__ __forceinline__ bool is_zero_row(const GatherArgs& g, const int32_t* 
   return j >= (int64_t)sb[e] - (e > 0 ? sb[e - 1] : 0);
 }
 
+#ifndef MOE_GATHER_MINB
+#define MOE_GATHER_MINB 4
+#endif
 template <int VB, int U, bool PADDED, typename ST>
-__global__ void __launch_bounds__(kThreads) gather_token_kernel(GatherArgs g) {
+__global__ void __launch_bounds__(kThreads, (std::is_void<ST>::value && VB == 32) ? MOE_GATHER_MINB : 1)
+gather_token_kernel(GatherArgs g) {
   constexpr bool kWeighted = !std::is_void<ST>::value;
   constexpr int KQ = 8;  // kept slots whose rows are written per sweep of the token row
   constexpr unsigned kAll = 0xffffffffu;
@@ -276,11 +282,12 @@ __global__ void __launch_bounds__(kThreads) gather_token_kernel(GatherArgs g) {
   const int64_t warps = (int64_t)gridDim.x * (blockDim.x / kWarp);
   const V* __restrict__ x = reinterpret_cast<const V*>(g.x);
   V* __restrict__ out = reinterpret_cast<V*>(g.out);
-  const int64_t items = g.T + g.row_begin;  // tokens, then the rows this kernel may zero-fill
+  const int64_t token_items = g.T * g.segs;
+  const int64_t items = token_items + g.row_begin;  // token segments, then the rows this kernel may zero-fill
   for (int64_t item = (int64_t)blockIdx.x * (blockDim.x / kWarp) + threadIdx.x / kWarp; item < items;
        item += warps) {
-    if (item >= g.T) {
-      const int64_t r = item - g.T;
+    if (item >= token_items) {
+      const int64_t r = item - token_items;
       if (is_zero_row<PADDED>(g, sb, spb, r)) {
         V* dst = out + r * g.vecs;
         const V z = zero_vec<V>();
@@ -288,10 +295,13 @@ __global__ void __launch_bounds__(kThreads) gather_token_kernel(GatherArgs g) {
       }
       continue;
     }
-    const V* src = x + item * g.vecs;
+    const int64_t t = item / g.segs;
+    const int64_t c_begin = (item - t * g.segs) * g.seg_len;
+    const int64_t c_end = min(c_begin + g.seg_len, g.vecs);
+    const V* src = x + t * g.vecs;
     for (int k0 = 0; k0 < g.top_k; k0 += kWarp) {
       // lane k resolves slot k0 + k; rows in the borrowed tail are left to the last pass
-      const int64_t a = item * g.top_k + k0 + lane;
+      const int64_t a = t * g.top_k + k0 + lane;
       int64_t row = -1;
       float w = 1.0f;
       if (k0 + lane < g.top_k) {
@@ -319,12 +329,12 @@ __global__ void __launch_bounds__(kThreads) gather_token_kernel(GatherArgs g) {
           dst[q] = out + (q < nq ? r : 0) * g.vecs;
           wq[q] = __shfl_sync(kAll, kw, (q0 + q) & (kWarp - 1));
         }
-        for (int64_t c0 = 0; c0 < g.vecs; c0 += kWarp * U) {
+        for (int64_t c0 = c_begin; c0 < c_end; c0 += kWarp * U) {
           V v[U];
 #pragma unroll
           for (int u = 0; u < U; ++u) {
             const int64_t c = c0 + u * kWarp + lane;
-            if (c < g.vecs) v[u] = ld_stream(src + c);
+            if (c < c_end) v[u] = ld_stream(src + c);
           }
 #pragma unroll
           for (int q = 0; q < KQ; ++q) {
@@ -333,9 +343,9 @@ __global__ void __launch_bounds__(kThreads) gather_token_kernel(GatherArgs g) {
               for (int u = 0; u < U; ++u) {
                 const int64_t c = c0 + u * kWarp + lane;
                 if constexpr (kWeighted) {
-                  if (c < g.vecs) st_stream(dst[q] + c, scale_vec<ST>(v[u], wq[q]));
+                  if (c < c_end) st_stream(dst[q] + c, scale_vec<ST>(v[u], wq[q]));
                 } else {
-                  if (c < g.vecs) st_stream(dst[q] + c, v[u]);
+                  if (c < c_end) st_stream(dst[q] + c, v[u]);
                 }
               }
             }
@@ -362,9 +372,21 @@ __global__ void __launch_bounds__(kThreads) gather_token_kernel(GatherArgs g) {
 #ifndef MOE_GATHER_TMA
 #define MOE_GATHER_TMA 1
 #endif
-constexpr int kTmaWarps = 4;
+#ifndef MOE_GATHER_SEGS
+#define MOE_GATHER_SEGS 1  // column segments per token, register pass
+#endif
+#ifndef MOE_TMA_SEGS
+#define MOE_TMA_SEGS 2  // column segments per token, bulk-copy pass (two items of a 14 KB row measured best)
+#endif
+#ifndef MOE_TMA_WARPS
+#define MOE_TMA_WARPS 4
+#endif
+constexpr int kTmaWarps = MOE_TMA_WARPS;
 constexpr int kTmaThreads = kTmaWarps * kWarp;
-constexpr int kTmaChunk = 8192;  // bytes per staged row chunk
+#ifndef MOE_TMA_CHUNK
+#define MOE_TMA_CHUNK 8192
+#endif
+constexpr int kTmaChunk = MOE_TMA_CHUNK;  // bytes per staged row chunk
 constexpr size_t kTmaSmem = (size_t)kTmaChunk * (1 + 2 * kTmaWarps) + 16 * kTmaWarps;
 constexpr int kSpinLimit = 1 << 22;
 
@@ -410,7 +432,7 @@ __device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wa
 __device__ __forceinline__ void fence_async_shared() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
 
 template <bool PADDED>
-__global__ void __launch_bounds__(kTmaThreads) gather_tma_kernel(GatherArgs g, int64_t row_bytes) {
+__global__ void __launch_bounds__(kTmaThreads, 1) gather_tma_kernel(GatherArgs g, int64_t row_bytes) {
   constexpr unsigned kAll = 0xffffffffu;
   extern __shared__ __align__(128) unsigned char tsm[];
   __shared__ int32_t sbins[kStageMax];
@@ -447,13 +469,14 @@ __global__ void __launch_bounds__(kTmaThreads) gather_tma_kernel(GatherArgs g, i
   }
 
   const int64_t warps = (int64_t)gridDim.x * kTmaWarps;
-  const int64_t items = g.T + g.row_begin;  // tokens, then the rows this kernel may zero-fill
+  const int64_t token_items = g.T * g.segs;
+  const int64_t items = token_items + g.row_begin;  // token segments, then the rows this kernel may zero-fill
   uint32_t parity = 0;                       // bit b: parity of buffer b's next completion
   int use = 0;                               // buffer of the next chunk
   bool ok = true;
   for (int64_t item = (int64_t)blockIdx.x * kTmaWarps + warp; item < items && ok; item += warps) {
-    if (item >= g.T) {
-      const int64_t r = item - g.T;
+    if (item >= token_items) {
+      const int64_t r = item - token_items;
       if (lane == 0 && is_zero_row<PADDED>(g, sb, spb, r)) {
         for (int64_t off = 0; off < row_bytes; off += kTmaChunk)
           bulk_store(g.out + r * row_bytes + off, smem_u32(zero), (uint32_t)min((int64_t)kTmaChunk, row_bytes - off));
@@ -461,8 +484,11 @@ __global__ void __launch_bounds__(kTmaThreads) gather_tma_kernel(GatherArgs g, i
       }
       continue;
     }
+    const int64_t t = item / g.segs;
+    const int64_t b_begin = (item - t * g.segs) * g.seg_len;
+    const int64_t b_end = min(b_begin + g.seg_len, row_bytes);
     for (int k0 = 0; k0 < g.top_k && ok; k0 += kWarp) {
-      const int64_t a = item * g.top_k + k0 + lane;
+      const int64_t a = t * g.top_k + k0 + lane;
       int64_t row = -1;
       if (k0 + lane < g.top_k) {
         const int32_t i = __ldg(g.positions + a);
@@ -478,14 +504,14 @@ __global__ void __launch_bounds__(kTmaThreads) gather_tma_kernel(GatherArgs g, i
       if (nk == 0) continue;
       const int from = lane < nk ? (int)__fns(kept, 0, lane + 1) : 0;
       const int64_t krow = __shfl_sync(kAll, row, from);  // lane q: row of the q-th kept slot
-      for (int64_t off = 0; off < row_bytes; off += kTmaChunk) {
-        const uint32_t bytes = (uint32_t)min((int64_t)kTmaChunk, row_bytes - off);
+      for (int64_t off = b_begin; off < b_end; off += kTmaChunk) {
+        const uint32_t bytes = (uint32_t)min((int64_t)kTmaChunk, b_end - off);
         const uint32_t buf = smem_u32(bufs + (size_t)use * kTmaChunk);
         const uint32_t bar = smem_u32(bars + use);
         bool got = true;
         if (lane == 0) {
           bulk_wait_read_but_one();  // the stores that last read this buffer have finished
-          bulk_load(buf, g.x + item * row_bytes + off, bytes, bar);
+          bulk_load(buf, g.x + t * row_bytes + off, bytes, bar);
           got = mbar_wait(bar, (parity >> use) & 1u);
           parity ^= 1u << use;
         }
@@ -522,8 +548,12 @@ bool launch_gather_tma(const GatherArgs& g, int64_t row_bytes, cudaStream_t s, i
     }
     if (dev >= 0 && dev < 64) configured[dev] = 1;
   }
-  const int64_t work_ctas = (g.T + g.row_begin + kTmaWarps - 1) / kTmaWarps;
-  k<<<persistent_grid(k, kTmaThreads, kTmaSmem, work_ctas), kTmaThreads, kTmaSmem, s>>>(g, row_bytes);
+  GatherArgs gt = g;
+  gt.segs = MOE_TMA_SEGS;
+  gt.seg_len = ((row_bytes + gt.segs - 1) / gt.segs + 15) / 16 * 16;  // bytes, 16-byte multiples
+  gt.segs = (row_bytes + gt.seg_len - 1) / gt.seg_len;
+  const int64_t work_ctas = (gt.T * gt.segs + gt.row_begin + kTmaWarps - 1) / kTmaWarps;
+  k<<<persistent_grid(k, kTmaThreads, kTmaSmem, work_ctas), kTmaThreads, kTmaSmem, s>>>(gt, row_bytes);
   *rc = check_launch();
   return true;
 }
@@ -532,17 +562,20 @@ template <int VB, bool PADDED, typename ST>
 int launch_gather(GatherArgs g, int64_t row_bytes, cudaStream_t s) {
   constexpr int U = VB == 32 ? 4 : (VB >= 8 ? 8 : 16);  // 128 bytes per lane in flight
   constexpr int kWarps = kThreads / kWarp;
-  // Borrow the last 4n bytes of the output (16-byte aligned) for the
-  // positions when the rows before them are at least some of the output.
+  g.segs = MOE_GATHER_SEGS;
+  g.seg_len = ((g.vecs + g.segs - 1) / g.segs + kWarp - 1) / kWarp * kWarp;  // vectors, whole warp passes
+  g.segs = g.seg_len > 0 ? (g.vecs + g.seg_len - 1) / g.seg_len : 1;
   if (g.positions != nullptr) {
     // The caller's positions (route build in the same call): one token pass over every row.
     g.row_begin = g.rows_out;
     int rc = MOE_OK;
     if (std::is_void<ST>::value && launch_gather_tma<PADDED>(g, row_bytes, s, &rc)) return rc;
     auto kt = gather_token_kernel<VB, U, PADDED, ST>;
-    kt<<<persistent_grid(kt, kThreads, 0, (g.T + g.row_begin + kWarps - 1) / kWarps), kThreads, 0, s>>>(g);
+    kt<<<persistent_grid(kt, kThreads, 0, (g.T * g.segs + g.row_begin + kWarps - 1) / kWarps), kThreads, 0, s>>>(g);
     return check_launch();
   }
+  // Borrow the last 4n bytes of the output (16-byte aligned) for the
+  // positions when the rows before them are at least some of the output.
   const uint64_t total = (uint64_t)g.rows_out * (uint64_t)row_bytes;
   const uint64_t need = 4ull * (uint64_t)g.n;
   g.row_begin = 0;
@@ -558,7 +591,7 @@ int launch_gather(GatherArgs g, int64_t row_bytes, cudaStream_t s) {
     int rc = MOE_OK;
     if (!(std::is_void<ST>::value && launch_gather_tma<PADDED>(g, row_bytes, s, &rc))) {
       auto kt = gather_token_kernel<VB, U, PADDED, ST>;
-      kt<<<persistent_grid(kt, kThreads, 0, (g.T + g.row_begin + kWarps - 1) / kWarps), kThreads, 0, s>>>(g);
+      kt<<<persistent_grid(kt, kThreads, 0, (g.T * g.segs + g.row_begin + kWarps - 1) / kWarps), kThreads, 0, s>>>(g);
       rc = check_launch();
     }
     if (rc != MOE_OK) return MOE_ERR_CUDA;

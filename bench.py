@@ -547,11 +547,12 @@ def time_sweeps(args, path, flush, stream) -> dict:
 
 def run_e2e(args, path, dev, dist):
     """The same step through the public API from pinned host buffers: every
-    step copies its inputs host->device, reads the padded row count back and
-    copies its combined outputs and router gradient device->host, all inside
-    the timed region. Copies run on their own streams and overlap the
-    neighbouring steps' kernels (step i+1's inputs go up and step i-1's
-    outputs come down while step i computes), as a serving loop would."""
+    step copies its inputs host->device and its combined outputs and router
+    gradient device->host, all inside the timed region. Copies run on their
+    own streams and overlap the neighbouring steps' kernels (step i+1's
+    inputs go up and step i-1's outputs come down while step i computes), as
+    a serving loop would; the padded path sizes its expert tensor by the
+    bound n + E*(m-1), so the host never waits inside a step."""
     import torch
 
     p, r = path.p, path.r
@@ -563,11 +564,10 @@ def run_e2e(args, path, dev, dist):
     h_out = {"yb": torch.empty_like(path.yb, device="cpu").pin_memory(),
              "yp": torch.empty_like(path.yp, device="cpu").pin_memory(),
              "gprobs": torch.empty_like(path.gprobs, device="cpu").pin_memory()}
-    h_p = torch.empty(1, dtype=torch.int32).pin_memory()
+    p_max = path.n + E * (r.pad_multiple - 1)
     d_in = [{k: torch.empty_like(v, device=dev) for k, v in h_in.items()} for _ in range(2)]
     ev_in = [torch.cuda.Event() for _ in range(2)]    # inputs of buffer b uploaded
     ev_used = [torch.cuda.Event() for _ in range(2)]  # the step on buffer b has finished with them
-    ev_p = torch.cuda.Event()
 
     def upload(i):
         b = i % 2
@@ -582,16 +582,15 @@ def run_e2e(args, path, dev, dist):
         din = d_in[b]
         sc.wait_event(ev_in[b])
         pi, idx = p.moe_routing_map_to_indices_fwd(din["probs"], din["rmap"], K)
-        rt = p.moe_route_build(idx, E, r.pad_multiple, workspace=path.ws)
-        h_p.copy_(rt.padded_bins[-1:], non_blocking=True)
-        ev_p.record(sc)
-        ev_p.synchronize()
-        P = int(h_p.item())
+        # route build + padded gather in one call, into the largest padded
+        # size n + E*(m-1): the host never waits for the data-dependent
+        # padded row count, so the copies of the neighbouring steps overlap
+        rt, xp = p.moe_route_build_padded_gather(idx, din["x"], E, r.pad_multiple, out_rows=p_max,
+                                                 workspace=path.ws)
         w = pi.view(-1)
         xb = p.moe_binned_gather(din["x"], rt.indices, rt.bins, E, r.capacity, K)
         yb = p.moe_binned_scatter(xb, rt.indices, rt.bin_ids, rt.bins, w, T, K, positions=rt.positions)
         p.moe_binned_wgrad(xb, din["grad"], rt.indices, rt.bin_ids, rt.bins, K)
-        xp = p.moe_padded_gather(din["x"], rt.indices, rt.bins, rt.padded_bins, K, out_rows=P)
         yp = p.moe_padded_scatter(xp, rt.indices, rt.bin_ids, rt.bins, rt.padded_bins, w, T, K,
                                   positions=rt.positions)
         wgp = p.moe_padded_wgrad(xp, din["grad"], rt.indices, rt.bin_ids, rt.bins, rt.padded_bins, K)
@@ -629,10 +628,11 @@ def run_e2e(args, path, dev, dist):
     ms = max_over_ranks(t0.elapsed_time(t1), dist, dev)
     world = dist.get_world_size() if dist is not None else 1
     h2d = sum(v.numel() * v.element_size() for v in h_in.values())
-    d2h = sum(v.numel() * v.element_size() for v in h_out.values()) + 4
+    d2h = sum(v.numel() * v.element_size() for v in h_out.values())
     return {"value": round(weak_scaling_value(world, path.n, steps, ms), 1), "unit": UNIT, "steps": steps,
             "ms_per_step": round(ms / steps, 5), "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-            "overlap": "copies on their own streams, overlapping the neighbouring steps' kernels"}
+            "overlap": "copies on their own streams, overlapping the neighbouring steps' kernels",
+            "padded_rows_allocated": p_max}
 
 
 # ------------------------------------------------------------------ CPU oracle

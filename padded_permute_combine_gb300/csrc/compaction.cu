@@ -8,9 +8,10 @@
 // each route its output slot in increasing expert order; the first topk are
 // emitted with their probabilities and the rest of the row is padded with
 // -1 / 0.0f.
-// Backward: one thread per group of four dense outputs, so the dense
-// gradient is written with full-width coalesced stores; each thread scans the
-// row's topk compact slots (cached in L1) for indices that fall in its group.
+// Backward: one warp per row when the row is whole float4s: the row's topk
+// compact slots are loaded once, broadcast by shuffles, and each lane writes
+// its four columns of every 128-column chunk with one float4 store; other
+// shapes take one thread per dense output, scanning the row's slots.
 #include "common.cuh"
 
 namespace moe {
@@ -129,6 +130,49 @@ __global__ void __launch_bounds__(kThreads)
   }
 }
 
+// Backward, one warp per row (E a multiple of 4, 16-byte aligned output):
+// lane j holds compact slot k0 + j; the slots are broadcast in increasing j
+// and each lane keeps the ones that fall in its four columns of the current
+// 128-column chunk (a repeated index keeps the highest j), then stores them
+// with one float4 store. Every dense element is written exactly once.
+__global__ void __launch_bounds__(kThreads)
+    compaction_bwd_warp_kernel(const float* __restrict__ gpi, const int32_t* __restrict__ indices, int64_t T,
+                               int32_t E, int32_t topk, float* __restrict__ grad_probs, int32_t* status) {
+  const int lane = lane_id();
+  const int64_t warps = (int64_t)gridDim.x * (blockDim.x / kWarp);
+  for (int64_t t = (int64_t)blockIdx.x * (blockDim.x / kWarp) + threadIdx.x / kWarp; t < T; t += warps) {
+    const int32_t* irow = indices + t * topk;
+    const float* grow = gpi + t * topk;
+    float4* drow = reinterpret_cast<float4*>(grad_probs + t * E);
+    bool bad = false;
+    for (int c0 = 0; c0 < E; c0 += 4 * kWarp) {
+      const int col = c0 + 4 * lane;  // first of this lane's four columns
+      float o0 = 0.0f, o1 = 0.0f, o2 = 0.0f, o3 = 0.0f;
+      for (int k0 = 0; k0 < topk; k0 += kWarp) {
+        const int nj = min(kWarp, topk - k0);
+        int32_t e = -1;
+        float v = 0.0f;
+        if (lane < nj) {
+          e = __ldg(irow + k0 + lane);
+          v = __ldg(grow + k0 + lane);
+          bad |= (e < -1 || e >= E);
+        }
+        for (int j = 0; j < nj; ++j) {
+          const int32_t ej = __shfl_sync(0xffffffffu, e, j);
+          const float vj = __shfl_sync(0xffffffffu, v, j);
+          const unsigned d = (unsigned)(ej - col);
+          if (d == 0u) o0 = vj;
+          if (d == 1u) o1 = vj;
+          if (d == 2u) o2 = vj;
+          if (d == 3u) o3 = vj;
+        }
+      }
+      if (col < E) drow[col / 4] = make_float4(o0, o1, o2, o3);
+    }
+    if (__any_sync(0xffffffffu, bad) && lane == 0) flag_status(status, MOE_STATUS_BAD_INDEX);
+  }
+}
+
 template <typename K>
 int grid_for(K k, int64_t work) {
   return persistent_grid(k, kThreads, 0, (work + kThreads - 1) / kThreads);
@@ -205,8 +249,8 @@ extern "C" int moe_routing_map_to_indices_bwd(const float* grad_probs_indices, c
   if (T == 0) return MOE_OK;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   if (E % 4 == 0 && aligned(grad_probs, 16)) {
-    auto k = compaction_bwd_kernel<4>;
-    k<<<grid_for(k, T * (E / 4)), kThreads, 0, s>>>(grad_probs_indices, indices, T, E, topk, grad_probs, d_status);
+    auto k = compaction_bwd_warp_kernel;
+    k<<<grid_for(k, T * kWarp), kThreads, 0, s>>>(grad_probs_indices, indices, T, E, topk, grad_probs, d_status);
   } else {
     auto k = compaction_bwd_kernel<1>;
     k<<<grid_for(k, T * E), kThreads, 0, s>>>(grad_probs_indices, indices, T, E, topk, grad_probs, d_status);

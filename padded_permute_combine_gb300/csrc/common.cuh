@@ -5,6 +5,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <utility>
+
 #include "moe_route.h"
 
 namespace moe {
@@ -166,6 +168,18 @@ __device__ __forceinline__ void two_sum(float a, float b, float& s, float& e) {
   e = __fadd_rn(__fsub_rn(a, __fsub_rn(s, bb)), __fsub_rn(b, bb));
 }
 
+// Programmatic dependent launch (every kernel of the library is launched
+// with it, see launch()): the kernel's grid may be launched while the
+// previous kernel on the stream is still finishing, so it waits here for
+// that kernel's results before its first global-memory access. No kernel
+// triggers its dependents early: the next grid launches as this one's CTAs
+// exit. (Triggering at kernel start let the next grid's CTAs settle on the
+// SMs unevenly while this one still ran, and the persistent grid-stride
+// kernels then lost more than the overlap gained: 1.11 vs 0.99 ms per
+// DeepSeek-V3-shaped routing step.) With a previous kernel that was
+// launched without the attribute, the wait is a no-op.
+__device__ __forceinline__ void await_previous_kernel() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 // ------------------------------------------------------------------ host
 
 int num_sms();       // SMs of the current device (cached per device)
@@ -183,6 +197,25 @@ inline int pick_vec_bytes(int64_t row_bytes, const void* const* ptrs, int nptrs,
     if (ok) return vb;
   }
   return 0;
+}
+
+// Launches `kernel` on `s` with programmatic stream serialization, so that
+// its launch overlaps the tail of the previous kernel (which the kernel
+// waits for in await_previous_kernel()). Errors surface through
+// cudaGetLastError like a <<<>>> launch.
+template <typename... KArgs, typename... Args>
+void launch(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  (void)cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
 }
 
 // Grid of CTAs for a grid-stride kernel: enough to fill every SM at the

@@ -57,6 +57,7 @@ template <int C>
 __global__ void __launch_bounds__(kThreads)
     compaction_fwd_kernel(const float* __restrict__ probs, const int8_t* __restrict__ rmap, int64_t T, int32_t E,
                           int32_t topk, float* __restrict__ probs_indices, int32_t* __restrict__ indices) {
+  await_previous_kernel();
   const int lane = lane_id();
   const int64_t warps = (int64_t)gridDim.x * (blockDim.x / kWarp);
   for (int64_t t = (int64_t)blockIdx.x * (blockDim.x / kWarp) + threadIdx.x / kWarp; t < T; t += warps) {
@@ -99,6 +100,7 @@ template <int G>
 __global__ void __launch_bounds__(kThreads)
     compaction_bwd_kernel(const float* __restrict__ gpi, const int32_t* __restrict__ indices, int64_t T, int32_t E,
                           int32_t topk, float* __restrict__ grad_probs, int32_t* status) {
+  await_previous_kernel();
   const int64_t groups_per_row = E / G;
   const int64_t total = T * groups_per_row;
   for (int64_t q = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; q < total; q += (int64_t)gridDim.x * blockDim.x) {
@@ -138,6 +140,7 @@ __global__ void __launch_bounds__(kThreads)
 __global__ void __launch_bounds__(kThreads)
     compaction_bwd_warp_kernel(const float* __restrict__ gpi, const int32_t* __restrict__ indices, int64_t T,
                                int32_t E, int32_t topk, float* __restrict__ grad_probs, int32_t* status) {
+  await_previous_kernel();
   const int lane = lane_id();
   const int64_t warps = (int64_t)gridDim.x * (blockDim.x / kWarp);
   for (int64_t t = (int64_t)blockIdx.x * (blockDim.x / kWarp) + threadIdx.x / kWarp; t < T; t += warps) {
@@ -206,31 +209,31 @@ extern "C" int moe_routing_map_to_indices_fwd(const float* probs, const int8_t* 
   switch (C) {
     case 16: {
       auto k = compaction_fwd_kernel<16>;
-      k<<<persistent_grid(k, kThreads, 0, work_ctas), kThreads, 0, s>>>(probs, routing_map, T, E, topk,
+      launch(k, persistent_grid(k, kThreads, 0, work_ctas), kThreads, 0, s, probs, routing_map, T, E, topk,
                                                                           probs_indices, indices);
       break;
     }
     case 8: {
       auto k = compaction_fwd_kernel<8>;
-      k<<<persistent_grid(k, kThreads, 0, work_ctas), kThreads, 0, s>>>(probs, routing_map, T, E, topk,
+      launch(k, persistent_grid(k, kThreads, 0, work_ctas), kThreads, 0, s, probs, routing_map, T, E, topk,
                                                                           probs_indices, indices);
       break;
     }
     case 4: {
       auto k = compaction_fwd_kernel<4>;
-      k<<<persistent_grid(k, kThreads, 0, work_ctas), kThreads, 0, s>>>(probs, routing_map, T, E, topk,
+      launch(k, persistent_grid(k, kThreads, 0, work_ctas), kThreads, 0, s, probs, routing_map, T, E, topk,
                                                                           probs_indices, indices);
       break;
     }
     case 2: {
       auto k = compaction_fwd_kernel<2>;
-      k<<<persistent_grid(k, kThreads, 0, work_ctas), kThreads, 0, s>>>(probs, routing_map, T, E, topk,
+      launch(k, persistent_grid(k, kThreads, 0, work_ctas), kThreads, 0, s, probs, routing_map, T, E, topk,
                                                                           probs_indices, indices);
       break;
     }
     default: {
       auto k = compaction_fwd_kernel<1>;
-      k<<<persistent_grid(k, kThreads, 0, work_ctas), kThreads, 0, s>>>(probs, routing_map, T, E, topk,
+      launch(k, persistent_grid(k, kThreads, 0, work_ctas), kThreads, 0, s, probs, routing_map, T, E, topk,
                                                                           probs_indices, indices);
     }
   }
@@ -250,10 +253,10 @@ extern "C" int moe_routing_map_to_indices_bwd(const float* grad_probs_indices, c
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   if (E % 4 == 0 && aligned(grad_probs, 16)) {
     auto k = compaction_bwd_warp_kernel;
-    k<<<grid_for(k, T * kWarp), kThreads, 0, s>>>(grad_probs_indices, indices, T, E, topk, grad_probs, d_status);
+    launch(k, grid_for(k, T * kWarp), kThreads, 0, s, grad_probs_indices, indices, T, E, topk, grad_probs, d_status);
   } else {
     auto k = compaction_bwd_kernel<1>;
-    k<<<grid_for(k, T * E), kThreads, 0, s>>>(grad_probs_indices, indices, T, E, topk, grad_probs, d_status);
+    launch(k, grid_for(k, T * E), kThreads, 0, s, grad_probs_indices, indices, T, E, topk, grad_probs, d_status);
   }
   return check_launch();
 }

@@ -123,6 +123,7 @@ __device__ __forceinline__ V scale_vec(const V& v, float w) {
 // weight of its assignment (the weighted gather).
 template <int VB, int U, bool PADDED, typename ST>
 __global__ void __launch_bounds__(kThreads) gather_kernel(GatherArgs g) {
+  await_previous_kernel();
   constexpr bool kWeighted = !std::is_void<ST>::value;
   using V = typename Vec<VB>::T;
   __shared__ int32_t sbins[kStageMax];
@@ -188,6 +189,7 @@ __global__ void __launch_bounds__(kThreads) gather_kernel(GatherArgs g) {
 
 __global__ void positions_kernel(const int32_t* __restrict__ indices, int64_t n, int32_t* __restrict__ positions,
                                  int32_t* status) {
+  await_previous_kernel();
   for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x) {
     const int32_t a = __ldg(indices + i);
     if (a >= 0 && a < n) positions[a] = (int32_t)i;
@@ -251,6 +253,7 @@ __device__ __forceinline__ bool is_zero_row(const GatherArgs& g, const int32_t* 
 template <int VB, int U, bool PADDED, typename ST>
 __global__ void __launch_bounds__(kThreads, (std::is_void<ST>::value && VB == 32) ? MOE_GATHER_MINB : 1)
 gather_token_kernel(GatherArgs g) {
+  await_previous_kernel();
   constexpr bool kWeighted = !std::is_void<ST>::value;
   constexpr int KQ = 8;  // kept slots whose rows are written per sweep of the token row
   constexpr unsigned kAll = 0xffffffffu;
@@ -433,6 +436,7 @@ __device__ __forceinline__ void fence_async_shared() { asm volatile("fence.proxy
 
 template <bool PADDED>
 __global__ void __launch_bounds__(kTmaThreads, 1) gather_tma_kernel(GatherArgs g, int64_t row_bytes) {
+  await_previous_kernel();
   constexpr unsigned kAll = 0xffffffffu;
   extern __shared__ __align__(128) unsigned char tsm[];
   __shared__ int32_t sbins[kStageMax];
@@ -553,7 +557,7 @@ bool launch_gather_tma(const GatherArgs& g, int64_t row_bytes, cudaStream_t s, i
   gt.seg_len = ((row_bytes + gt.segs - 1) / gt.segs + 15) / 16 * 16;  // bytes, 16-byte multiples
   gt.segs = (row_bytes + gt.seg_len - 1) / gt.seg_len;
   const int64_t work_ctas = (gt.T * gt.segs + gt.row_begin + kTmaWarps - 1) / kTmaWarps;
-  k<<<persistent_grid(k, kTmaThreads, kTmaSmem, work_ctas), kTmaThreads, kTmaSmem, s>>>(gt, row_bytes);
+  launch(k, persistent_grid(k, kTmaThreads, kTmaSmem, work_ctas), kTmaThreads, kTmaSmem, s, gt, row_bytes);
   *rc = check_launch();
   return true;
 }
@@ -571,7 +575,7 @@ int launch_gather(GatherArgs g, int64_t row_bytes, cudaStream_t s) {
     int rc = MOE_OK;
     if (std::is_void<ST>::value && launch_gather_tma<PADDED>(g, row_bytes, s, &rc)) return rc;
     auto kt = gather_token_kernel<VB, U, PADDED, ST>;
-    kt<<<persistent_grid(kt, kThreads, 0, (g.T * g.segs + g.row_begin + kWarps - 1) / kWarps), kThreads, 0, s>>>(g);
+    launch(kt, persistent_grid(kt, kThreads, 0, (g.T * g.segs + g.row_begin + kWarps - 1) / kWarps), kThreads, 0, s, g);
     return check_launch();
   }
   // Borrow the last 4n bytes of the output (16-byte aligned) for the
@@ -585,19 +589,19 @@ int launch_gather(GatherArgs g, int64_t row_bytes, cudaStream_t s) {
     g.positions = reinterpret_cast<const int32_t*>(p);
     g.row_begin = (int64_t)((p - base) / (uint64_t)row_bytes);  // rows wholly before the positions
     const int64_t blocks = (g.n + 255) / 256;
-    positions_kernel<<<(unsigned)(blocks < 4096 ? blocks : 4096), 256, 0, s>>>(
+    launch(positions_kernel, (unsigned)(blocks < 4096 ? blocks : 4096), 256, 0, s, 
         g.indices, g.n, reinterpret_cast<int32_t*>(p), g.status);
     if (check_launch() != MOE_OK) return MOE_ERR_CUDA;
     int rc = MOE_OK;
     if (!(std::is_void<ST>::value && launch_gather_tma<PADDED>(g, row_bytes, s, &rc))) {
       auto kt = gather_token_kernel<VB, U, PADDED, ST>;
-      kt<<<persistent_grid(kt, kThreads, 0, (g.T * g.segs + g.row_begin + kWarps - 1) / kWarps), kThreads, 0, s>>>(g);
+      launch(kt, persistent_grid(kt, kThreads, 0, (g.T * g.segs + g.row_begin + kWarps - 1) / kWarps), kThreads, 0, s, g);
       rc = check_launch();
     }
     if (rc != MOE_OK) return MOE_ERR_CUDA;
   }
   auto k = gather_kernel<VB, U, PADDED, ST>;  // rows [row_begin, rows_out), destination-major
-  k<<<persistent_grid(k, kThreads, 0, (g.rows_out - g.row_begin + kWarps - 1) / kWarps), kThreads, 0, s>>>(g);
+  launch(k, persistent_grid(k, kThreads, 0, (g.rows_out - g.row_begin + kWarps - 1) / kWarps), kThreads, 0, s, g);
   return check_launch();
 }
 

@@ -28,6 +28,7 @@ template <int NPL>
 __global__ void __launch_bounds__(kThreads)
     gating_kernel(const float* __restrict__ logits, int64_t T, int32_t E, int32_t K, int32_t mode, int32_t normalize,
                   int32_t* __restrict__ top_expert, float* __restrict__ weights) {
+  await_previous_kernel();
   const int lane = lane_id();
   const int64_t warps = (int64_t)gridDim.x * (blockDim.x / kWarp);
   for (int64_t t = (int64_t)blockIdx.x * (blockDim.x / kWarp) + threadIdx.x / kWarp; t < T; t += warps) {
@@ -121,7 +122,7 @@ int launch_gating(const float* logits, int64_t T, int32_t E, int32_t K, int32_t 
                   int32_t* top_expert, float* weights, cudaStream_t s) {
   auto k = gating_kernel<NPL>;
   const int64_t work_ctas = (T + (kThreads / kWarp) - 1) / (kThreads / kWarp);
-  k<<<persistent_grid(k, kThreads, 0, work_ctas), kThreads, 0, s>>>(logits, T, E, K, mode, normalize, top_expert,
+  launch(k, persistent_grid(k, kThreads, 0, work_ctas), kThreads, 0, s, logits, T, E, K, mode, normalize, top_expert,
                                                                       weights);
   return check_launch();
 }

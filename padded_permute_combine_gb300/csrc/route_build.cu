@@ -50,6 +50,7 @@ __device__ __forceinline__ int32_t load_expert(const int32_t* top_expert, int64_
 
 __global__ void route_hist_kernel(const int32_t* __restrict__ top_expert, int64_t n, int32_t E,
                                   int32_t* __restrict__ counts, int32_t* status) {
+  await_previous_kernel();
   extern __shared__ int32_t hist[];
   for (int e = threadIdx.x; e < E; e += blockDim.x) hist[e] = 0;
   __syncthreads();
@@ -70,6 +71,7 @@ __global__ void route_hist_kernel(const int32_t* __restrict__ top_expert, int64_
 __global__ void __launch_bounds__(kScanThreads) route_scan_kernel(int32_t* __restrict__ counts, int64_t G, int32_t E,
                                                                    int32_t m, int32_t* __restrict__ bins,
                                                                    int32_t* __restrict__ padded_bins) {
+  await_previous_kernel();
   __shared__ int32_t start[MOE_MAX_EXPERTS];
   __shared__ int64_t warp_sum[kScanThreads / kWarp][2];
   // Column pass: exclusive prefix over chunks, total per expert.
@@ -146,6 +148,7 @@ __global__ void __launch_bounds__(kScanThreads) route_scan_kernel(int32_t* __res
 __global__ void route_scatter_kernel(const int32_t* __restrict__ top_expert, int64_t n, int32_t E,
                                      const int32_t* __restrict__ offsets, int32_t* __restrict__ indices,
                                      int32_t* __restrict__ bin_ids, int32_t* __restrict__ positions) {
+  await_previous_kernel();
   extern __shared__ int32_t whist[];  // [warps][E]: per-warp running offsets
   const int warps = blockDim.x / kWarp;
   const int warp = threadIdx.x / kWarp, lane = lane_id();
@@ -218,10 +221,10 @@ extern "C" int moe_route_build(const int32_t* top_expert, int64_t n, int32_t E, 
   const RouteShape shape = route_shape(n, E);
   int32_t* counts = static_cast<int32_t*>(workspace);
   const int threads = shape.warps * kWarp;
-  route_hist_kernel<<<(unsigned)shape.ctas, threads, E * sizeof(int32_t), s>>>(top_expert, n, E, counts, d_status);
-  route_scan_kernel<<<1, kScanThreads, 0, s>>>(counts, shape.ctas, E, pad_multiple, bins, padded_bins);
+  launch(route_hist_kernel, (unsigned)shape.ctas, threads, E * sizeof(int32_t), s, top_expert, n, E, counts, d_status);
+  launch(route_scan_kernel, 1, kScanThreads, 0, s, counts, shape.ctas, E, pad_multiple, bins, padded_bins);
   if (n > 0)
-    route_scatter_kernel<<<(unsigned)shape.ctas, threads, (size_t)shape.warps * E * sizeof(int32_t), s>>>(
+    launch(route_scatter_kernel, (unsigned)shape.ctas, threads, (size_t)shape.warps * E * sizeof(int32_t), s, 
         top_expert, n, E, counts, indices, bin_ids, positions);
   return check_launch();
 }

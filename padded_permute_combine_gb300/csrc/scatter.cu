@@ -192,6 +192,7 @@ constexpr int64_t kSegTarget = 256;  // vectors per work item, at most
 
 template <int VB, typename ET, bool PADDED, bool WEIGHTED>
 __global__ void __launch_bounds__(kThreads, kMinBlocks) scatter_kernel(ScatterArgs g) {
+  await_previous_kernel();
   using L = Lanes<VB, ET>;
   using V = typename L::V;
   constexpr int NE = L::kElems;
@@ -344,6 +345,7 @@ __device__ __forceinline__ void stream_kept_async(const uint4* __restrict__ xe, 
 // per SM); the padded one (8 rows per token) measured faster without the cap.
 template <typename ET, bool PADDED, bool WEIGHTED>
 __global__ void __launch_bounds__(kAsyncThreads, PADDED ? 1 : 6) scatter_async_kernel(ScatterArgs g) {
+  await_previous_kernel();
   __shared__ uint4 ring_all[kAsyncWarps * kAsyncSlots * kWarp];
   const int lane = lane_id();
   uint4* ring = ring_all + (threadIdx.x / kWarp) * kAsyncSlots * kWarp;
@@ -380,6 +382,7 @@ __global__ void __launch_bounds__(kAsyncThreads, PADDED ? 1 : 6) scatter_async_k
 
 __global__ void invert_kernel(const int32_t* __restrict__ indices, int64_t n, int32_t* __restrict__ positions,
                               int32_t* status) {
+  await_previous_kernel();
   for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x) {
     const int32_t a = __ldg(indices + i);
     if (a >= 0 && a < n) positions[a] = (int32_t)i;
@@ -399,10 +402,10 @@ int launch_scatter(ScatterArgs g, cudaStream_t s) {
       const int64_t actas = (g.T * g.segs + kAsyncWarps - 1) / kAsyncWarps;
       if (g.weights != nullptr) {
         auto k = scatter_async_kernel<ET, PADDED, true>;
-        k<<<persistent_grid(k, kAsyncThreads, 0, actas), kAsyncThreads, 0, s>>>(g);
+        launch(k, persistent_grid(k, kAsyncThreads, 0, actas), kAsyncThreads, 0, s, g);
       } else {
         auto k = scatter_async_kernel<ET, PADDED, false>;
-        k<<<persistent_grid(k, kAsyncThreads, 0, actas), kAsyncThreads, 0, s>>>(g);
+        launch(k, persistent_grid(k, kAsyncThreads, 0, actas), kAsyncThreads, 0, s, g);
       }
       return check_launch();
     }
@@ -410,10 +413,10 @@ int launch_scatter(ScatterArgs g, cudaStream_t s) {
   const int64_t work_ctas = (g.T * g.segs + (kThreads / kWarp) - 1) / (kThreads / kWarp);
   if (g.weights != nullptr) {
     auto k = scatter_kernel<VB, ET, PADDED, true>;
-    k<<<persistent_grid(k, kThreads, 0, work_ctas), kThreads, 0, s>>>(g);
+    launch(k, persistent_grid(k, kThreads, 0, work_ctas), kThreads, 0, s, g);
   } else {
     auto k = scatter_kernel<VB, ET, PADDED, false>;
-    k<<<persistent_grid(k, kThreads, 0, work_ctas), kThreads, 0, s>>>(g);
+    launch(k, persistent_grid(k, kThreads, 0, work_ctas), kThreads, 0, s, g);
   }
   return check_launch();
 }
@@ -432,7 +435,7 @@ int run_scatter(ScatterArgs g, int32_t dtype, const int32_t* indices, void* work
       return MOE_ERR_INVALID_ARG;
     int32_t* pos = static_cast<int32_t*>(workspace);
     const int64_t blocks = (g.n + 255) / 256;
-    invert_kernel<<<(unsigned)(blocks < 4096 ? blocks : 4096), 256, 0, s>>>(indices, g.n, pos, g.status);
+    launch(invert_kernel, (unsigned)(blocks < 4096 ? blocks : 4096), 256, 0, s, indices, g.n, pos, g.status);
     if (check_launch() != MOE_OK) return MOE_ERR_CUDA;
     g.positions = pos;
   }

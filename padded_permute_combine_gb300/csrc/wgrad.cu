@@ -103,6 +103,7 @@ __device__ __forceinline__ int32_t ld_position(const int32_t* p) {
 // pass reads each slot once and then overwrites it with the result.
 __global__ void positions_kernel(const int32_t* __restrict__ indices, int64_t n, int32_t* positions,
                                  int32_t* status) {
+  await_previous_kernel();
   for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x) {
     const int32_t a = __ldg(indices + i);
     if (a >= 0 && a < n) positions[a] = (int32_t)i;
@@ -181,6 +182,7 @@ __device__ __forceinline__ int64_t sorted_row(const WgradArgs& g, int64_t i, int
 //    rows are loaded evict-last for their later slots.
 template <int VB, int U, typename ET, bool PADDED, bool BY_ASSIGNMENT>
 __global__ void __launch_bounds__(kThreads) wgrad_kernel(WgradArgs g) {
+  await_previous_kernel();
   using L = Lanes<VB, ET>;
   using V = typename L::V;
   constexpr int NE = L::kElems;
@@ -257,14 +259,14 @@ int launch_wgrad(const WgradArgs& g, cudaStream_t s) {
   constexpr bool kByAssignment = PADDED;
   if (kByAssignment) {
     const int64_t blocks = (g.n + 255) / 256;
-    positions_kernel<<<(unsigned)(blocks < 4096 ? blocks : 4096), 256, 0, s>>>(
+    launch(positions_kernel, (unsigned)(blocks < 4096 ? blocks : 4096), 256, 0, s, 
         g.indices, g.n, reinterpret_cast<int32_t*>(g.wgrad), g.status);
     if (check_launch() != MOE_OK) return MOE_ERR_CUDA;
   }
   constexpr int U = VB == 32 ? 2 : (VB == 16 ? 4 : 8);  // 64 bytes per lane and operand in flight
   auto k = wgrad_kernel<VB, U, ET, PADDED, kByAssignment>;
   const int64_t work_ctas = (g.n + (kThreads / kWarp) - 1) / (kThreads / kWarp);
-  k<<<persistent_grid(k, kThreads, 0, work_ctas), kThreads, 0, s>>>(g);
+  launch(k, persistent_grid(k, kThreads, 0, work_ctas), kThreads, 0, s, g);
   return check_launch();
 }
 

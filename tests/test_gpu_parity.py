@@ -178,11 +178,13 @@ def test_deepseek_v3_capacity_factor_and_padding_multiple(capacity_factor, pad_m
 
 # ------------------------------------------------------------ route build + gather in one call
 
-def run_fused(r: wl.Routing, binned=True, padded=True):
+def run_fused(r: wl.Routing, binned=True, padded=True, misalign=False):
     """The one-call route build + gather against the oracle's route build and
     gathers: all five route outputs and the gathered tensor, bit for bit."""
     E, m = r.E, r.pad_multiple or 1
     te, x = to_dev(r.top_expert, DEV), to_dev(r.x, DEV)
+    if misalign:
+        x = misaligned_like(x)  # off the 16-byte rule: the register copy path
     o = oracle.route_build(r.top_expert, E, m)
     st = status_word()
     if binned:
@@ -210,6 +212,8 @@ def test_fused_route_gather_tiny_and_edges():
     run_fused(wl.uniform_routing("fused-k33", 29, 24, 48, 33, wl.BF16, capacity=5, pad_multiple=8, seed=33))
     run_fused(wl.uniform_routing("fused-h7", 37, 7, 6, 2, wl.BF16, capacity=9, pad_multiple=4, seed=7))
     run_fused(wl.uniform_routing("fused-t1", 1, 40, 4, 2, wl.F32, capacity=1, pad_multiple=2, seed=7))
+    run_fused(wl.uniform_routing("fused-mis", 40, 64, 6, 2, wl.BF16, capacity=10, pad_multiple=4, seed=9),
+              misalign=True)
     r = wl.zipf_routing("fused-cap0", 300, 40, 16, 4, wl.F32, pad_multiple=3, seed=5)
     r.capacity = 0
     run_fused(r, padded=False)
@@ -272,6 +276,14 @@ def test_one_token_and_ragged_chunks():
     run_routing(wl.uniform_routing("t1", 1, 40, 4, 2, wl.F32, capacity=1, pad_multiple=2, seed=7))
     # n not a multiple of any block size; many route-build chunks
     run_routing(wl.zipf_routing("ragged", 2053, 16, 64, 3, wl.BF16, capacity=50, pad_multiple=32, seed=8))
+
+
+def test_more_experts_than_staged_bins():
+    # E above the 1024 experts whose bins the kernels stage in shared memory:
+    # bins and padded_bins are read from global memory instead
+    r = wl.zipf_routing("e3000", 700, 24, 3000, 4, wl.BF16, capacity=2, pad_multiple=4, seed=13)
+    run_routing(r)
+    run_fused(r)
 
 
 def test_no_tokens():

@@ -63,6 +63,7 @@ _SIGS = {
     "oracle_topk_gating": [_VP, _I64, _I32, _I32, _INT, _INT, _VP, _VP],
     "oracle_binned_gather_weighted": [_VP, _INT, _VP, _VP, _VP, _VP, _I64, _I64, _I32, _I32, _I32, _VP],
     "oracle_padded_gather_weighted": [_VP, _INT, _VP, _VP, _VP, _VP, _VP, _I64, _I64, _I32, _I32, _VP, _I64],
+    "oracle_check_routing": [_VP, _VP, _VP, _VP, _VP, _I64, _I32],
 }
 
 
@@ -115,6 +116,15 @@ def route_build(top_expert, E: int, pad_multiple: int = 1, lib=None):
                                 _p(out["bins"]), _p(out["padded_bins"]), _p(out["positions"]))
     _check(rc, "route_build")
     return out
+
+
+def check_routing(indices, bin_ids, bins, padded_bins=None, positions=None, lib=None) -> int:
+    """Status bits of the routing check (0 = consistent)."""
+    lib = lib or load()
+    idx, bid, b = _i32(indices), _i32(bin_ids), _i32(bins)
+    pb = None if padded_bins is None else _i32(padded_bins)
+    pos = None if positions is None else _i32(positions)
+    return int(lib.oracle_check_routing(_p(idx), _p(bid), _p(b), _p(pb), _p(pos), idx.size, b.size))
 
 
 def binned_gather(x, indices, bin_ids, bins, E, capacity, top_k, lib=None):

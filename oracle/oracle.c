@@ -167,6 +167,51 @@ static int check_bins(const int32_t* indices, const int32_t* bin_ids, const int3
 }
 
 /*
+ * Routing check ([binned] Guardrails: bins monotonic, bins[-1] ==
+ * len(indices), bin_ids aligned with the bin boundaries; [padded]
+ * Guardrails: padded segments no shorter than the real counts; [padded]
+ * Workflow step 1: assignments sorted by expert, in increasing id within an
+ * expert). Returns the OR of status bits, 0 for a consistent routing:
+ *   4 (bins):   bins[0] < 0, bins decreasing, bins[E-1] != n, padded_bins
+ *               decreasing or a padded segment shorter than its count,
+ *               sorted position i outside the segment of bin_ids[i];
+ *   1 (expert): bin_ids[i] outside [0, E);
+ *   2 (index):  indices[i] outside [0, n), indices not increasing inside a
+ *               run of equal bin_ids, or (positions given)
+ *               positions[indices[i]] != i.
+ * Every condition is tested for every element; nothing stops early.
+ */
+int oracle_check_routing(const int32_t* indices, const int32_t* bin_ids, const int32_t* bins,
+                         const int32_t* padded_bins, const int32_t* positions, int64_t n, int32_t E) {
+    int bits = 0;
+    for (int32_t e = 0; e < E; ++e) {
+        int64_t start = seg_start(bins, e);
+        if (bins[e] < start || (e == 0 && bins[0] < 0)) bits |= 4;
+        if (padded_bins) {
+            int64_t pstart = seg_start(padded_bins, e);
+            if (padded_bins[e] < pstart || padded_bins[e] - pstart < (int64_t)bins[e] - start) bits |= 4;
+        }
+    }
+    if (E > 0 && bins[E - 1] != n) bits |= 4;
+    for (int64_t i = 0; i < n; ++i) {
+        int32_t e = bin_ids[i];
+        if (e < 0 || e >= E) {
+            bits |= 1;
+        } else if (i < seg_start(bins, e) || i >= bins[e]) {
+            bits |= 4;
+        }
+        int32_t a = indices[i];
+        if (a < 0 || a >= n) {
+            bits |= 2;
+        } else if (positions && positions[a] != i) {
+            bits |= 2;
+        }
+        if (i > 0 && bin_ids[i] == bin_ids[i - 1] && a <= indices[i - 1]) bits |= 2;
+    }
+    return bits;
+}
+
+/*
  * Gather ([binned] Goal, Workflow step 3, Guardrails; [padded] Goal,
  * Workflow steps 4-5, Guardrails). out has out_rows rows of H elements:
  * E*capacity rows (binned, padded_bins == NULL) or padded_bins[E-1] rows

@@ -520,6 +520,55 @@ def check_golden(lib):
     assert gp.tolist() == c["grad_probs"]
 
 
+def check_routing_golden(lib):
+    """The routing check on the hand-worked cases of routing_check_worked.txt,
+    with and without positions and padded_bins."""
+    c = read_golden("routing_check_worked.txt")
+    base = {k: c[k] for k in ("indices", "bin_ids", "bins", "padded_bins", "positions")}
+    assert oracle.check_routing(**base, lib=lib) == 0
+    for name, case in c.items():
+        if not isinstance(case, dict):
+            continue
+        v = dict(base)
+        v.update({k: case[k] for k in base if k in case})
+        assert oracle.check_routing(**v, lib=lib) == case["bits"], name
+        assert oracle.check_routing(v["indices"], v["bin_ids"], v["bins"], lib=lib) == case["bits_np"], name
+
+
+def check_routing_properties(lib):
+    """The routing check on the routes of the (separately pinned) route
+    build: 0 with and without positions and padded_bins; exchanging two
+    entries of positions sets bit 2 only when positions are given;
+    reversing a segment of two or more entries sets bit 2; bins[0] above
+    bins[1] sets bit 4; bins[E-1] one past n sets bit 4."""
+    for te, E, K in _routings():
+        for m in (1, 3):
+            o = oracle.route_build(te, E, m, lib=lib)
+            idx, bid, bins, pb, pos = o["indices"], o["bin_ids"], o["bins"], o["padded_bins"], o["positions"]
+            n = idx.size
+            assert oracle.check_routing(idx, bid, bins, pb, pos, lib=lib) == 0
+            assert oracle.check_routing(idx, bid, bins, lib=lib) == 0
+            if n >= 2:
+                p2 = pos.copy()
+                p2[0], p2[n - 1] = p2[n - 1], p2[0]
+                assert oracle.check_routing(idx, bid, bins, pb, p2, lib=lib) == 2
+                assert oracle.check_routing(idx, bid, bins, pb, lib=lib) == 0
+            starts = np.concatenate([[0], bins[:-1]])
+            long_seg = [e for e in range(E) if bins[e] - starts[e] >= 2]
+            if long_seg:
+                e = long_seg[0]
+                i2 = idx.copy()
+                i2[starts[e]:bins[e]] = i2[starts[e]:bins[e]][::-1]
+                assert oracle.check_routing(i2, bid, bins, lib=lib) == 2
+            if E >= 2 and n > 0:
+                b2 = bins.copy()
+                b2[0] = b2[1] + 1
+                assert oracle.check_routing(idx, bid, b2, lib=lib) & 4
+            b3 = bins.copy()
+            b3[E - 1] = n + 1
+            assert oracle.check_routing(idx, bid, b3, lib=lib) == 4
+
+
 ALL_CHECKS = [
     check_golden,
     check_route_invariants,
@@ -536,4 +585,6 @@ ALL_CHECKS = [
     check_bruteforce,
     check_bf16_rounding,
     check_bf16_golden,
+    check_routing_golden,
+    check_routing_properties,
 ]

@@ -66,6 +66,9 @@ MUTANTS = [
     ("wgather_unscaled", "float scaled = weights ? weights[a] * v : v;", "float scaled = weights ? v : v;"),
     ("wgather_token_mod", "int64_t a = indices[i];\n        int64_t token = a / top_k;",
      "int64_t a = indices[i];\n        int64_t token = a % top_k;"),
+    ("check_ignores_positions", "} else if (positions && positions[a] != i) {", "} else if (0) {"),
+    ("check_no_order", "if (i > 0 && bin_ids[i] == bin_ids[i - 1] && a <= indices[i - 1]) bits |= 2;", ""),
+    ("check_no_end", "if (E > 0 && bins[E - 1] != n) bits |= 4;", ""),
 ]
 
 _RUNNER = textwrap.dedent("""

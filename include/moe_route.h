@@ -148,6 +148,30 @@ int moe_route_build_noalloc(const int32_t* top_expert, int64_t n,
                             int32_t* d_status, moe_stream_t stream);
 
 /*
+ * Routing check ([binned] Guardrails: bins monotonic, bins[-1] == n, bin_ids
+ * aligned with the bin boundaries; [padded] Guardrails: padded segments no
+ * shorter than the counts; [padded] Workflow step 1: sorted by expert, in
+ * increasing assignment id within an expert). ORs into *d_status (the
+ * caller zeroes it first; required):
+ *   MOE_STATUS_BAD_BINS    bins[0] < 0, bins decreasing, bins[E-1] != n,
+ *                          padded_bins decreasing or a padded segment shorter
+ *                          than its count, or a sorted position outside the
+ *                          segment of its bin_ids entry;
+ *   MOE_STATUS_BAD_EXPERT  a bin_ids entry outside [0, E);
+ *   MOE_STATUS_BAD_INDEX   an indices entry outside [0, n), indices not
+ *                          increasing inside a run of equal bin_ids, or
+ *                          (positions given) positions[indices[i]] != i —
+ *                          with positions this certifies that indices is a
+ *                          permutation.
+ *   indices, bin_ids [n]; bins [E]; padded_bins [E] and positions [n]
+ *   nullable (their conditions are then skipped). One launch, no host sync.
+ */
+int moe_check_routing(const int32_t* indices, const int32_t* bin_ids,
+                      const int32_t* bins, const int32_t* padded_bins,
+                      const int32_t* positions, int64_t n, int32_t num_experts,
+                      int32_t* d_status, moe_stream_t stream);
+
+/*
  * Binned gather ([binned] Goal, Workflow step 3, Implementation Pattern,
  * Guardrails). For expert e and slot j < capacity:
  *   out[e, j, :] = x[indices[bins[e-1] + j] / top_k, :]  if j < count_e,

@@ -9,6 +9,7 @@ from .ops import (  # noqa: F401
     moe_binned_gather_weighted,
     moe_binned_scatter,
     moe_binned_wgrad,
+    moe_check_routing,
     moe_padded_gather,
     moe_padded_gather_weighted,
     moe_padded_scatter,

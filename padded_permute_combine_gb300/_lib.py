@@ -34,6 +34,7 @@ SIGNATURES = {
     "moe_route_build_workspace_size": (_SZ, [_I64, _I32]),
     "moe_route_build": (ctypes.c_int, [_P, _I64, _I32, _I32, _P, _P, _P, _P, _P, _P, _SZ, _P, _P]),
     "moe_route_build_noalloc": (ctypes.c_int, [_P, _I64, _I32, _I32, _P, _P, _P, _P, _P, _P, _P]),
+    "moe_check_routing": (ctypes.c_int, [_P, _P, _P, _P, _P, _I64, _I32, _P, _P]),
     "moe_binned_gather": (ctypes.c_int, [_P, _I32, _P, _P, _I64, _I64, _I32, _I32, _I32, _P, _P, _P]),
     "moe_padded_gather": (ctypes.c_int, [_P, _I32, _P, _P, _P, _I64, _I64, _I32, _I32, _P, _I64, _P, _P]),
     "moe_binned_gather_weighted": (ctypes.c_int, [_P, _I32, _P, _P, _P, _I64, _I64, _I32, _I32, _I32, _P, _P, _P]),

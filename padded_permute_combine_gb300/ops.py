@@ -78,6 +78,27 @@ def moe_route_build(top_expert: torch.Tensor, num_experts: int, pad_multiple: in
     return out
 
 
+def moe_check_routing(indices: torch.Tensor, bin_ids: torch.Tensor, bins: torch.Tensor,
+                      padded_bins: torch.Tensor | None = None, positions: torch.Tensor | None = None,
+                      status: torch.Tensor | None = None) -> torch.Tensor:
+    """Consistency check of a routing; returns the device status word
+    (int32 [1], zeroed here unless given) with MOE_STATUS_* bits OR-ed in."""
+    _need(indices, torch.int32, "indices")
+    dev = indices.device
+    _need(bin_ids, torch.int32, "bin_ids", dev)
+    _need(bins, torch.int32, "bins", dev)
+    if padded_bins is not None:
+        _need(padded_bins, torch.int32, "padded_bins", dev)
+    if positions is not None:
+        _need(positions, torch.int32, "positions", dev)
+    if status is None:
+        status = torch.zeros(1, dtype=torch.int32, device=dev)
+    _need(status, torch.int32, "status", dev)
+    _lib.call("moe_check_routing", _ptr(indices), _ptr(bin_ids), _ptr(bins), _ptr(padded_bins), _ptr(positions),
+              indices.numel(), bins.numel(), _ptr(status), _stream(indices))
+    return status
+
+
 def moe_binned_gather(x: torch.Tensor, indices: torch.Tensor, bins: torch.Tensor, num_experts: int,
                       capacity: int, top_k: int, out: torch.Tensor | None = None,
                       status: torch.Tensor | None = None) -> torch.Tensor:

@@ -18,7 +18,7 @@ def lib():
 
 def test_header_and_exports_agree(lib):
     declared = _lib.header_functions()
-    assert len(declared) == len(set(declared)) == 19
+    assert len(declared) == len(set(declared)) == 20
     out = subprocess.run(["nm", "-D", "--defined-only", _lib.LIB_PATH], capture_output=True, text=True,
                          check=True).stdout
     exported = {ln.split()[-1] for ln in out.splitlines() if " T " in ln}
@@ -93,6 +93,11 @@ def test_host_validation_rejects_bad_arguments(lib):
                                              FAKE, ws2, None, None) == 1
     assert lib.moe_route_build_padded_gather(FAKE, FAKE, 1, 4, 8, 2, 2, 4, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, -1,
                                              FAKE, ws2, None, None) == 1
+    # routing check: status word required, E out of range, negative n, misaligned bins
+    assert lib.moe_check_routing(FAKE, FAKE, FAKE, None, None, 8, 2, None, None) == 1
+    assert lib.moe_check_routing(FAKE, FAKE, FAKE, None, None, 8, 0, FAKE, None) == 1
+    assert lib.moe_check_routing(FAKE, FAKE, FAKE, None, None, -1, 2, FAKE, None) == 1
+    assert lib.moe_check_routing(FAKE, FAKE, FAKE + 2, None, None, 8, 2, FAKE, None) == 2
     # gating: top_k above E, bad mode, E above the gating limit
     assert lib.moe_topk_gating(FAKE, 4, 8, 9, 0, 1, FAKE, FAKE, None) == 1
     assert lib.moe_topk_gating(FAKE, 4, 8, 2, 5, 1, FAKE, FAKE, None) == 1

@@ -2,6 +2,7 @@
 (permute), scatter (combine), router-weight gradient and the dense
 routing-map compaction, as hand-written sm_103a CUDA kernels behind the C ABI
 in include/moe_route.h, with a thin Python binding of the same names."""
+from . import autograd  # noqa: F401
 from ._lib import MoeError, load  # noqa: F401
 from .ops import (  # noqa: F401
     Route,

@@ -42,6 +42,7 @@ METRIC = "routed rows/sec and achieved HBM GB/s (% of GB300 peak), gather+scatte
 UNIT = "rows/s"
 L2_FLUSH_BYTES = 512 << 20
 FALLBACK_HBM_GBS = 6800.0
+NOMINAL_HBM_GBS = 8000.0  # the GB300's nominal HBM3e bandwidth, reported beside the measured peak
 # the csrc/ translation unit each timed kernel is compiled from
 KERNEL_UNIT = {"compaction_fwd": "compaction", "compaction_bwd": "compaction", "route_build": "route_build",
                "binned_gather": "gather", "padded_gather": "gather", "binned_scatter": "scatter",
@@ -431,7 +432,8 @@ def run_gpu(args, rank, world, local_rank):
         ms = statistics.mean(per_kernel[name])
         gbs = algo[name] / (ms * 1e-3) / 1e9
         kern[name] = {"ms": round(ms, 5), "algorithmic_bytes": algo[name], "gbs": round(gbs, 1),
-                      "frac_of_%s_peak" % peak_kind: round(gbs / peak, 4), "launches": launches}
+                      "frac_of_%s_peak" % peak_kind: round(gbs / peak, 4),
+                      "frac_of_nominal_8tbs": round(gbs / NOMINAL_HBM_GBS, 4), "launches": launches}
         if name in survey:
             kern[name]["survey_bytes"] = survey[name]
             kern[name]["survey_gbs"] = round(survey[name] / (ms * 1e-3) / 1e9, 1)
@@ -680,6 +682,26 @@ def _sample_tokens(r, d, budget_s):
     return int(max(64, min(r.T, 256 * budget_s / dt)))
 
 
+def host_cpu_model() -> str:
+    """The host CPU's model string (lscpu, else /proc/cpuinfo, else the ISA)."""
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.startswith("Model name:"):
+                return line.split(":", 1)[1].strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    try:
+        for line in open("/proc/cpuinfo"):
+            if line.lower().startswith(("model name", "cpu part")):
+                return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    import platform
+
+    return platform.machine()
+
+
 def cpu_baseline(budget_s: float):
     import oracle
 
@@ -693,6 +715,7 @@ def cpu_baseline(budget_s: float):
         passes += 1
     dt = time.perf_counter() - t0
     return {"value": round(rows / dt, 1), "unit": UNIT, "cores": 1, "kind": "oracle",
+            "host_cpus": os.cpu_count(), "host_cpu": host_cpu_model(),
             "sample": "first %d of %d tokens of the same batch (capacity ceil(T*K/E)), full path, %d passes, "
                       "single-threaded C oracle, %.1f s" % (T_s, r.T, passes, dt)}
 
@@ -721,7 +744,8 @@ def run_reference(args, rank):
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(dt / args.steps * 1e3, 3),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
             "config": workload_config(r),
-            "cpu_baseline": {"value": round(value, 1), "unit": UNIT, "cores": 1, "kind": "oracle", "sample": sample},
+            "cpu_baseline": {"value": round(value, 1), "unit": UNIT, "cores": 1, "kind": "oracle", "sample": sample,
+                             "host_cpus": os.cpu_count(), "host_cpu": host_cpu_model()},
             "e2e": {"value": round(value, 1), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
 

@@ -479,7 +479,32 @@ def time_next_rows(args, path, flush, stream):
     for name, fn, nbytes in path.next_ops():
         out[name] = time_alone(args, fn, nbytes, flush, stream)
     out.update(time_sweeps(args, path, flush, stream))
+    out.update(time_compaction_workload(args, path, flush, stream))
     return out
+
+
+def time_compaction_workload(args, path, flush, stream) -> dict:
+    """The compaction forward and backward on their own named workload, the
+    Qwen2-MoE-57B-shaped dense routing map (T=65536, E=64, topk=8), each
+    launch timed alone."""
+    import torch
+
+    p, dev = path.p, path.dev
+    d = wl.qwen2_moe_57b()
+    T, E, k = d.probs.shape[0], d.probs.shape[1], d.topk
+    probs = torch.from_numpy(d.probs).to(dev)
+    rmap = torch.from_numpy(d.routing_map).to(dev)
+    gpi = torch.from_numpy(d.grad_probs_indices).to(dev)
+    pi = torch.empty((T, k), dtype=torch.float32, device=dev)
+    idx = torch.empty((T, k), dtype=torch.int32, device=dev)
+    gp = torch.empty((T, E), dtype=torch.float32, device=dev)
+    p.moe_routing_map_to_indices_fwd(probs, rmap, k, out=(pi, idx))
+    return {"qwen2_moe_57b_compaction": {
+        "tokens": T, "experts": E, "topk": k,
+        "fwd": time_alone(args, lambda: p.moe_routing_map_to_indices_fwd(probs, rmap, k, out=(pi, idx)),
+                          T * E + T * k * 4 + T * k * 8, flush, stream),
+        "bwd": time_alone(args, lambda: p.moe_routing_map_to_indices_bwd(gpi, idx, E, out=gp),
+                          T * k * 8 + T * E * 4, flush, stream)}}
 
 
 def time_alone(args, fn, nbytes, flush, stream) -> dict:

@@ -280,10 +280,10 @@ class Path:
         }
 
 
-    def survey_bytes(self) -> dict:
-        """The per-kernel byte counts of the survey's measurement plan, which
-        count a token row once per kept slot in the gathers and a gradient
-        row once per kept slot in wgrad (a schedule without row reuse)."""
+    def no_reuse_bytes(self) -> dict:
+        """Per-kernel byte counts of a schedule without row reuse: a token
+        row once per kept slot in the gathers and a gradient row once per
+        kept slot in wgrad (the row-granular plan the kernels started from)."""
         r = self.r
         T, H, E, n, b = r.T, r.H, r.E, self.n, 2
         kept, P, cap = self.kept, self.P, r.capacity
@@ -426,7 +426,7 @@ def run_gpu(args, rank, world, local_rank):
     value = weak_scaling_value(world, n, args.steps, total_ms)
     peak, peak_kind = measured_peak()
     algo = path.algorithmic_bytes()
-    survey = path.survey_bytes()
+    no_reuse = path.no_reuse_bytes()
     kern = {}
     for name, launches, _ in ops:
         ms = statistics.mean(per_kernel[name])
@@ -434,9 +434,9 @@ def run_gpu(args, rank, world, local_rank):
         kern[name] = {"ms": round(ms, 5), "algorithmic_bytes": algo[name], "gbs": round(gbs, 1),
                       "frac_of_%s_peak" % peak_kind: round(gbs / peak, 4),
                       "frac_of_nominal_8tbs": round(gbs / NOMINAL_HBM_GBS, 4), "launches": launches}
-        if name in survey:
-            kern[name]["survey_bytes"] = survey[name]
-            kern[name]["survey_gbs"] = round(survey[name] / (ms * 1e-3) / 1e9, 1)
+        if name in no_reuse:
+            kern[name]["no_reuse_bytes"] = no_reuse[name]
+            kern[name]["no_reuse_gbs"] = round(no_reuse[name] / (ms * 1e-3) / 1e9, 1)
     hot = ["binned_gather", "binned_scatter", "binned_wgrad", "padded_gather", "padded_scatter", "padded_wgrad"]
     hot_bytes = sum(algo[k] for k in hot)
     hot_ms = sum(kern[k]["ms"] for k in hot)

@@ -8,10 +8,14 @@
 // each route its output slot in increasing expert order; the first topk are
 // emitted with their probabilities and the rest of the row is padded with
 // -1 / 0.0f.
-// Backward: one warp per row when the row is whole float4s: the row's topk
-// compact slots are loaded once, broadcast by shuffles, and each lane writes
-// its four columns of every 128-column chunk with one float4 store; other
-// shapes take one thread per dense output, scanning the row's slots.
+// Rows of at most 64 experts with topk <= 8 take one thread per row instead
+// (32 rows per warp in flight).
+// Backward: one thread per 16 dense columns when rows are whole 16-column
+// chunks and topk <= 8 (the row's slots loaded once, four float4 stores of
+// zeros, the slots stored over them);
+// else one warp per row when the row is whole float4s (slots broadcast by
+// shuffles, one float4 store per lane and 128-column chunk); other shapes
+// take one thread per dense output, scanning the row's slots.
 #include "common.cuh"
 
 namespace moe {
@@ -91,6 +95,100 @@ __global__ void __launch_bounds__(kThreads)
     for (int j = emitted + lane; j < topk; j += kWarp) {
       io[j] = -1;
       po[j] = 0.0f;
+    }
+  }
+}
+
+// Forward, one thread per token row, for maps of at most 64 experts in whole
+// 16-byte vectors and topk <= 8 (the Qwen2-MoE-57B shape: E = 64, topk = 8):
+// the row's NV map vectors give a 64-bit route mask, the first topk routes
+// in increasing expert order are taken from it, and their probabilities are
+// loaded together before the row's outputs are stored. A warp handles 32
+// rows at once instead of one.
+template <int NV>
+__global__ void __launch_bounds__(kThreads)
+    compaction_fwd_row_kernel(const float* __restrict__ probs, const int8_t* __restrict__ rmap, int64_t T, int32_t E,
+                              int32_t topk, float* __restrict__ probs_indices, int32_t* __restrict__ indices,
+                              bool vec_out) {
+  await_previous_kernel();
+  for (int64_t t = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; t < T; t += (int64_t)gridDim.x * blockDim.x) {
+    const uint4* mrow = reinterpret_cast<const uint4*>(rmap + t * E);
+    uint64_t mask = 0;
+#pragma unroll
+    for (int v = 0; v < NV; ++v) {
+      const uint4 w = __ldg(mrow + v);
+      const uint64_t m16 = nonzero_bytes(w.x) | (nonzero_bytes(w.y) << 4) | (nonzero_bytes(w.z) << 8) |
+                           (nonzero_bytes(w.w) << 12);
+      mask |= m16 << (16 * v);
+    }
+    int32_t e[8];
+    float p[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      e[j] = -1;
+      if (j < topk && mask != 0ull) {
+        e[j] = __ffsll((long long)mask) - 1;
+        mask &= mask - 1ull;
+      }
+    }
+#pragma unroll
+    for (int j = 0; j < 8; ++j) p[j] = e[j] >= 0 ? __ldg(probs + t * E + e[j]) : 0.0f;
+    float* po = probs_indices + t * topk;
+    int32_t* io = indices + t * topk;
+    if (vec_out) {  // topk == 8, rows 16-byte aligned
+      reinterpret_cast<float4*>(po)[0] = make_float4(p[0], p[1], p[2], p[3]);
+      reinterpret_cast<float4*>(po)[1] = make_float4(p[4], p[5], p[6], p[7]);
+      reinterpret_cast<int4*>(io)[0] = make_int4(e[0], e[1], e[2], e[3]);
+      reinterpret_cast<int4*>(io)[1] = make_int4(e[4], e[5], e[6], e[7]);
+    } else {
+#pragma unroll
+      for (int j = 0; j < 8; ++j)
+        if (j < topk) {
+          po[j] = p[j];
+          io[j] = e[j];
+        }
+    }
+  }
+}
+
+// Backward, one thread per 16 dense columns of a row (E a multiple of 16,
+// 16-byte aligned output, topk <= 8): the row's compact slots are loaded
+// once (the row's other threads hit L1), the 16 columns are zeroed with four
+// float4 stores, and the slots that fall in them are stored over the zeros.
+__global__ void __launch_bounds__(kThreads)
+    compaction_bwd_chunk_kernel(const float* __restrict__ gpi, const int32_t* __restrict__ indices, int64_t T,
+                                int32_t E, int32_t topk, float* __restrict__ grad_probs, int32_t* status) {
+  await_previous_kernel();
+  const int64_t chunks = E / 16;
+  const int64_t total = T * chunks;
+  for (int64_t q = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; q < total; q += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t t = q / chunks;
+    const int c0 = (int)(q - t * chunks) * 16;
+    int32_t e[8];
+    float v[8];
+    bool bad = false;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      e[j] = -1;
+      v[j] = 0.0f;
+      if (j < topk) {
+        e[j] = __ldg(indices + t * topk + j);
+        v[j] = __ldg(gpi + t * topk + j);
+        bad |= (e[j] < -1 || e[j] >= E);
+      }
+    }
+    if (bad && c0 == 0) flag_status(status, MOE_STATUS_BAD_INDEX);
+    // zeros first, then the slots that land here in increasing slot order:
+    // the same thread's later store wins, so a repeated index keeps the
+    // highest slot
+    float* row = grad_probs + t * E + c0;
+    float4* dst = reinterpret_cast<float4*>(row);
+#pragma unroll
+    for (int u = 0; u < 4; ++u) dst[u] = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const unsigned d = (unsigned)(e[j] - c0);
+      if (d < 16u) row[d] = v[j];
     }
   }
 }
@@ -195,6 +293,21 @@ extern "C" int moe_routing_map_to_indices_fwd(const float* probs, const int8_t* 
   if (!aligned(probs, 4) || !aligned(probs_indices, 4) || !aligned(indices, 4)) return MOE_ERR_UNSUPPORTED;
   if (T == 0) return MOE_OK;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (E <= 64 && E % 16 == 0 && topk <= 8 && aligned(routing_map, 16)) {
+    const bool vec_out = topk == 8 && aligned(probs_indices, 16) && aligned(indices, 16);
+    const int64_t ctas = (T + kThreads - 1) / kThreads;
+    auto run = [&](auto k) {
+      launch(k, persistent_grid(k, kThreads, 0, ctas), kThreads, 0, s, probs, routing_map, T, E, topk, probs_indices,
+             indices, vec_out);
+    };
+    switch (E / 16) {
+      case 1: run(compaction_fwd_row_kernel<1>); break;
+      case 2: run(compaction_fwd_row_kernel<2>); break;
+      case 3: run(compaction_fwd_row_kernel<3>); break;
+      default: run(compaction_fwd_row_kernel<4>);
+    }
+    return check_launch();
+  }
   // Bytes per lane: the widest C in {16, 8, 4, 2} that divides E, keeps every
   // map row aligned to C and leaves at most half of the warp idle; else one
   // byte at a time.
@@ -251,7 +364,10 @@ extern "C" int moe_routing_map_to_indices_bwd(const float* grad_probs_indices, c
     return MOE_ERR_UNSUPPORTED;
   if (T == 0) return MOE_OK;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  if (E % 4 == 0 && aligned(grad_probs, 16)) {
+  if (E % 16 == 0 && topk <= 8 && aligned(grad_probs, 16)) {
+    auto k = compaction_bwd_chunk_kernel;
+    launch(k, grid_for(k, T * (E / 16)), kThreads, 0, s, grad_probs_indices, indices, T, E, topk, grad_probs, d_status);
+  } else if (E % 4 == 0 && aligned(grad_probs, 16)) {
     auto k = compaction_bwd_warp_kernel;
     launch(k, grid_for(k, T * kWarp), kThreads, 0, s, grad_probs_indices, indices, T, E, topk, grad_probs, d_status);
   } else {

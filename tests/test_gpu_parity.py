@@ -335,7 +335,8 @@ def test_qwen2_moe_57b_compaction():
 
 
 @pytest.mark.parametrize("T,E,topk,max_routes", [(1, 1, 1, 1), (333, 5, 3, 5), (1000, 64, 8, 12), (257, 160, 6, 6),
-                                                 (100, 37, 40, 37), (513, 256, 8, 8)])
+                                                 (100, 37, 40, 37), (513, 256, 8, 8), (777, 48, 5, 9),
+                                                 (300, 16, 8, 16), (65, 32, 2, 32)])
 def test_compaction_shapes(T, E, topk, max_routes):
     run_compaction(wl.dense_routes("c", T, E, topk, max_routes=max_routes, seed=T + E))
 

@@ -4,11 +4,12 @@
 //
 // Three launches, no inter-CTA waiting:
 //   1. hist:    CTA g counts the expert ids of its chunk -> counts[g][e].
-//   2. scan:    one CTA turns counts into per-(chunk, expert) start offsets
-//               (exclusive over experts, then over chunks) and writes bins
-//               and padded_bins.
+//   2. scan:    one CTA turns each expert's column of counts into a prefix
+//               over chunks and writes bins and padded_bins.
 //   3. scatter: CTA g re-reads its chunk and gives every assignment its
-//               stable rank: warps own consecutive sub-chunks, a warp-level
+//               stable rank (expert start bins[e-1] + the chunk prefix +
+//               the rank inside the chunk): warps own consecutive
+//               sub-chunks, a warp-level
 //               multi-split (__match_any_sync + popc of lower peers) ranks
 //               lanes within a round, and per-warp running counters in
 //               shared memory carry ranks across rounds and warps.
@@ -66,8 +67,10 @@ __global__ void route_hist_kernel(const int32_t* __restrict__ top_expert, int64_
   for (int e = threadIdx.x; e < E; e += blockDim.x) counts[(int64_t)blockIdx.x * E + e] = hist[e];
 }
 
-// Single CTA. counts[g][e] becomes the first sorted position of chunk g's
-// assignments to expert e.
+// Single CTA. counts[g][e] becomes the number of expert-e assignments in the
+// chunks before g (a column prefix); bins and padded_bins are written. The
+// scatter pass adds expert e's start, bins[e-1], to get the first sorted
+// position of chunk g's assignments to e.
 __global__ void __launch_bounds__(kScanThreads) route_scan_kernel(int32_t* __restrict__ counts, int64_t G, int32_t E,
                                                                    int32_t m, int32_t* __restrict__ bins,
                                                                    int32_t* __restrict__ padded_bins) {
@@ -132,21 +135,15 @@ __global__ void __launch_bounds__(kScanThreads) route_scan_kernel(int32_t* __res
   int64_t prun = xps - ps + (warp > 0 ? warp_sum[warp - 1][1] : 0);
   for (int e = lo; e < hi; ++e) {
     const int64_t c = start[e];
-    start[e] = (int32_t)run;  // now the exclusive start of expert e
     run += c;
     prun += (c + m - 1) / m * m;
     bins[e] = (int32_t)run;
     if (padded_bins != nullptr) padded_bins[e] = (int32_t)prun;
   }
-  __syncthreads();
-  for (int e = threadIdx.x; e < E; e += blockDim.x) {
-    const int32_t st = start[e];
-    for (int64_t g = 0; g < G; ++g) counts[g * E + e] += st;
-  }
 }
 
 __global__ void route_scatter_kernel(const int32_t* __restrict__ top_expert, int64_t n, int32_t E,
-                                     const int32_t* __restrict__ offsets, int32_t* __restrict__ indices,
+                                     const int32_t* __restrict__ offsets, const int32_t* __restrict__ bins, int32_t* __restrict__ indices,
                                      int32_t* __restrict__ bin_ids, int32_t* __restrict__ positions) {
   await_previous_kernel();
   extern __shared__ int32_t whist[];  // [warps][E]: per-warp running offsets
@@ -166,7 +163,7 @@ __global__ void route_scatter_kernel(const int32_t* __restrict__ top_expert, int
   }
   __syncthreads();
   for (int e = threadIdx.x; e < E; e += blockDim.x) {
-    int32_t run = offsets[(int64_t)blockIdx.x * E + e];
+    int32_t run = offsets[(int64_t)blockIdx.x * E + e] + (e > 0 ? bins[e - 1] : 0);
     for (int w = 0; w < warps; ++w) {
       const int32_t c = whist[w * E + e];
       whist[w * E + e] = run;
@@ -224,7 +221,7 @@ extern "C" int moe_route_build(const int32_t* top_expert, int64_t n, int32_t E, 
   launch(route_hist_kernel, (unsigned)shape.ctas, threads, E * sizeof(int32_t), s, top_expert, n, E, counts, d_status);
   launch(route_scan_kernel, 1, kScanThreads, 0, s, counts, shape.ctas, E, pad_multiple, bins, padded_bins);
   if (n > 0)
-    launch(route_scatter_kernel, (unsigned)shape.ctas, threads, (size_t)shape.warps * E * sizeof(int32_t), s, 
-        top_expert, n, E, counts, indices, bin_ids, positions);
+    launch(route_scatter_kernel, (unsigned)shape.ctas, threads, (size_t)shape.warps * E * sizeof(int32_t), s,
+           top_expert, n, E, counts, bins, indices, bin_ids, positions);
   return check_launch();
 }

@@ -1,6 +1,7 @@
 """The C-ABI library loads on the CPU, exports every function that
 include/moe_route.h declares, and rejects bad arguments on the host (before
 any CUDA call, so no GPU is needed)."""
+import os
 import re
 import subprocess
 
@@ -136,3 +137,20 @@ def test_product_path_has_no_oracle_dependency():
 def test_loader_fails_loudly_without_the_library(tmp_path):
     with pytest.raises(RuntimeError, match="not built"):
         _lib.load(str(tmp_path / "missing.so"))
+
+
+def test_header_is_plain_c(tmp_path):
+    """include/moe_route.h compiles as C11 in a plain C host (no C++, no
+    torch): the C host under tests/c_abi builds with gcc -c."""
+    import shutil
+    import subprocess
+
+    gcc = shutil.which("gcc")
+    if gcc is None:
+        pytest.skip("gcc not found")
+    here = os.path.dirname(os.path.abspath(__file__))
+    root = os.path.dirname(here)
+    cuda = os.environ.get("CUDA_HOME", "/usr/local/cuda")
+    subprocess.run([gcc, "-std=c11", "-Wall", "-Werror", "-c", "-I", os.path.join(root, "include"), "-I",
+                    os.path.join(cuda, "include"), os.path.join(here, "c_abi", "route_and_gather.c"), "-o",
+                    str(tmp_path / "host.o")], check=True)

@@ -321,7 +321,9 @@ int moe_padded_scatter(const void* xe, int32_t dtype, const int32_t* indices,
  * inverse permutation of indices in wgrad itself (n 32-bit slots), the
  * second reads each slot once and overwrites it with the result, visiting
  * assignments in id order so that each gradient row is read about once.
- * moe_binned_wgrad is one launch over sorted positions. wgrad must not
+ * moe_binned_wgrad is one launch: for E <= 1024 its warps visit only the
+ * kept rows (a thread per sorted position writes the dropped slots' 0),
+ * otherwise every sorted position. wgrad must not
  * alias any input; its contents are meaningful only once the call's work
  * has run. In the padded call a position that does not map back to its
  * assignment (indices not a permutation) sets MOE_STATUS_BAD_INDEX and that

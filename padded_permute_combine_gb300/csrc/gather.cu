@@ -23,6 +23,7 @@
 // each copied row by its assignment's weight on the way through.
 #include "common.cuh"
 #include "vec_math.cuh"
+#include "bulk.cuh"
 
 #include <type_traits>
 
@@ -391,48 +392,6 @@ constexpr int kTmaThreads = kTmaWarps * kWarp;
 #endif
 constexpr int kTmaChunk = MOE_TMA_CHUNK;  // bytes per staged row chunk
 constexpr size_t kTmaSmem = (size_t)kTmaChunk * (1 + 2 * kTmaWarps) + 16 * kTmaWarps;
-constexpr int kSpinLimit = 1 << 22;
-
-__device__ __forceinline__ uint32_t smem_u32(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
-
-__device__ __forceinline__ void mbar_init(uint32_t bar) {
-  asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(bar) : "memory");
-}
-
-// Expect `bytes` on the barrier, then copy global -> shared; completion
-// arrives on the barrier.
-__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
-  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
-  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
-               "l"(src), "r"(bytes), "r"(bar)
-               : "memory");
-}
-
-// Polls the barrier's phase with the given parity at most kSpinLimit times.
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
-  for (int it = 0; it < kSpinLimit; ++it) {
-    uint32_t done;
-    asm volatile(
-        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}"
-        : "=r"(done)
-        : "r"(bar), "r"(parity)
-        : "memory");
-    if (done) return true;
-  }
-  return false;
-}
-
-__device__ __forceinline__ void bulk_store(void* dst, uint32_t src, uint32_t bytes) {
-  asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(dst), "r"(src), "r"(bytes)
-               : "memory");
-}
-__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
-// Waits until at most one committed group still reads shared memory.
-__device__ __forceinline__ void bulk_wait_read_but_one() {
-  asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
-}
-__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
-__device__ __forceinline__ void fence_async_shared() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
 
 template <bool PADDED>
 __global__ void __launch_bounds__(kTmaThreads, 1) gather_tma_kernel(GatherArgs g, int64_t row_bytes) {
@@ -457,7 +416,7 @@ __global__ void __launch_bounds__(kTmaThreads, 1) gather_tma_kernel(GatherArgs g
       if (PADDED) spbins[e] = __ldg(g.padded_bins + e);
     }
   }
-  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  fence_mbarrier_init();
   fence_async_shared();  // the zero chunk and the barriers, for the bulk-copy unit
   __syncthreads();
   const int32_t* sb = staged ? sbins : g.bins;

@@ -4,15 +4,19 @@
 //  "Build Triton-Ascend Padded MoE Routing": Workflow step 6, Guardrails on
 //  unique assignment ids and reductions across column tiles).
 //
-// Two launches. The first writes the inverse permutation of `indices` into
-// the caller's wgrad buffer (it has exactly n 32-bit slots), so no workspace
-// is needed. The second gives one warp one assignment at a time in
-// assignment order, so the TOP_K assignments of a token run on neighbouring
-// warps and share the token's gradient row through L1: each gradient row
-// leaves HBM about once instead of once per kept slot, and each kept expert
-// row is read once. Each dot product is formed in fp32 with compensated
-// summation (Ogita, Rump and Oishi, "Accurate Sum and Dot Product", SIAM J.
-// Sci. Comput. 26(6), 2005, algorithm Dot2): every product and every partial
+// Padded layout, two launches: the first writes the inverse permutation of
+// `indices` into the caller's wgrad buffer (it has exactly n 32-bit slots),
+// so no workspace is needed; the second gives one warp one assignment at a
+// time in assignment order, so the TOP_K assignments of a token run on
+// neighbouring warps and share the token's gradient row through L1: each
+// gradient row leaves HBM about once, each expert row once. Binned layout,
+// one launch: capacity drops a contiguous tail of every expert's bin, so
+// the warps walk only the kept rows, in row order, and a thread-per-slot
+// pass writes the dropped slots' 0.
+//
+// Each dot product is formed in fp32 with compensated summation (Ogita, Rump
+// and Oishi, "Accurate Sum and Dot Product", SIAM J. Sci. Comput. 26(6),
+// 2005, algorithm Dot2): every product and every partial
 // sum carries its exact rounding error (TwoProduct via fma, Knuth's TwoSum),
 // the errors are summed separately and added once at the end, and the warp
 // reduction combines (sum, error) pairs the same way. For bf16 rows the
@@ -180,14 +184,69 @@ __device__ __forceinline__ int64_t sorted_row(const WgradArgs& g, int64_t i, int
 //  - otherwise sorted positions in increasing order, so kept expert rows are
 //    read in address order and the positions pass is not needed; gradient
 //    rows are loaded evict-last for their later slots.
-template <int VB, int U, typename ET, bool PADDED, bool BY_ASSIGNMENT>
-__global__ void __launch_bounds__(kThreads) wgrad_kernel(WgradArgs g) {
-  await_previous_kernel();
+// Compensated dot product of one expert row and one gradient row (vecs
+// vectors each), summed by the whole warp; every lane returns the result.
+// L1_GRAD: the gradient row goes through L1 (neighbouring warps read the
+// same row); otherwise it is loaded evict-last for its later readers.
+template <int VB, int U, typename ET, bool L1_GRAD>
+__device__ __forceinline__ float row_dot(const typename Lanes<VB, ET>::V* __restrict__ xr,
+                                         const typename Lanes<VB, ET>::V* __restrict__ gv, int64_t vecs, int lane) {
   using L = Lanes<VB, ET>;
   using V = typename L::V;
   constexpr int NE = L::kElems;
   constexpr bool kExact = Elem<ET>::kBytes == 2;  // bf16 x bf16 fits in fp32
   constexpr bool kPacked = kExact && NE % 2 == 0;
+  Acc2 acc[2];
+  Acc2x2 acc2[2];
+  auto load = [&](V (&vx)[U], V (&vg)[U], int64_t c0) {
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int64_t c = c0 + u * kWarp + lane;
+      if (c < vecs) {
+        vx[u] = ld_once(xr + c);  // each expert row is read once
+        vg[u] = L1_GRAD ? ld_l1(gv + c) : ld_keep(gv + c);
+      }
+    }
+  };
+  auto add = [&](const V (&vx)[U], const V (&vg)[U], int64_t c0) {
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int64_t c = c0 + u * kWarp + lane;
+      if (c < vecs) {
+        if constexpr (kPacked) {
+#pragma unroll
+          for (int p = 0; p < NE / 2; ++p)
+            acc2[p & 1].add_exact(f2_mul(f2_elems<ET>(vx[u], p), f2_elems<ET>(vg[u], p)));
+        } else {
+#pragma unroll
+          for (int q = 0; q < NE; ++q) acc[q & 1].template add_product<kExact>(L::get(vx[u], q), L::get(vg[u], q));
+        }
+      }
+    }
+  };
+  for (int64_t c0 = 0; c0 < vecs; c0 += kWarp * U) {
+    V vx[U], vg[U];
+    load(vx, vg, c0);
+    add(vx, vg, c0);
+  }
+  if constexpr (kPacked) {
+    acc2[0].fold_into(acc[0]);
+    acc2[1].fold_into(acc[1]);
+  }
+  acc[0].merge(acc[1].s, acc[1].c);
+#pragma unroll
+  for (int d = kWarp / 2; d > 0; d >>= 1) {
+    const float s2 = __shfl_xor_sync(0xffffffffu, acc[0].s, d);
+    const float c2 = __shfl_xor_sync(0xffffffffu, acc[0].c, d);
+    acc[0].merge(s2, c2);
+  }
+  return __fadd_rn(acc[0].s, acc[0].c);
+}
+
+template <int VB, int U, typename ET, bool PADDED, bool BY_ASSIGNMENT>
+__global__ void __launch_bounds__(kThreads) wgrad_kernel(WgradArgs g) {
+  await_previous_kernel();
+  using V = typename Lanes<VB, ET>::V;
   const int lane = lane_id();
   const int64_t warps = (int64_t)gridDim.x * (blockDim.x / kWarp);
   const V* __restrict__ xe = reinterpret_cast<const V*>(g.xe);
@@ -205,65 +264,171 @@ __global__ void __launch_bounds__(kThreads) wgrad_kernel(WgradArgs g) {
     row = __shfl_sync(0xffffffffu, row, 0);
     a = __shfl_sync(0xffffffffu, a, 0);
     if (row < 0) continue;
-    const V* xr = xe + row * g.vecs;
-    const V* gv = gr + (a / g.top_k) * g.vecs;
-    Acc2 acc[2];
-    Acc2x2 acc2[2];
-    for (int64_t c0 = 0; c0 < g.vecs; c0 += kWarp * U) {
-      V vx[U], vg[U];
+    const float r = row_dot<VB, U, ET, BY_ASSIGNMENT>(xe + row * g.vecs, gr + (a / g.top_k) * g.vecs, g.vecs, lane);
+    if (lane == 0) g.wgrad[a] = r;
+  }
+}
+
+// Binned rows, kept slots only. Capacity drops a contiguous tail of each
+// expert's bin, so the kept slots are the first min(count_e, capacity)
+// rows of each expert: each CTA stages bins and the prefix sums of the kept
+// counts in shared memory, and the warps walk kept slots k = 0 .. kept-1 in
+// row order (expert e by binary search on the prefix, then row e*capacity +
+// j, sorted position bins[e-1] + j), resolving 32 of them at once (one per
+// lane, their index loads overlapping). Dropped slots never reach a warp:
+// a grid-stride pass over the sorted positions, one thread each, writes
+// their 0 first. The data checks of the sorted walk are kept: bins
+// decreasing or past n, a bin_ids entry that disagrees with bins, an
+// indices entry outside [0, n).
+constexpr int kKeptStage = 1024;  // experts whose bins fit the shared-memory stage
+
+template <int VB, int U, typename ET>
+__global__ void __launch_bounds__(kThreads, 4) wgrad_kept_kernel(WgradArgs g) {
+  await_previous_kernel();
+  using V = typename Lanes<VB, ET>::V;
+  constexpr unsigned kAll = 0xffffffffu;
+  constexpr int kPer = kKeptStage / kThreads;
+  __shared__ int32_t sbins[kKeptStage];
+  __shared__ int32_t skept[kKeptStage];
+  __shared__ int32_t swarp[kThreads / kWarp];
+  __shared__ int64_t srow[kThreads];
+  __shared__ int32_t sa[kThreads];
+  const int tid = threadIdx.x, lane = lane_id(), warp = tid / kWarp;
+  for (int e = tid; e < g.E; e += kThreads) sbins[e] = __ldg(g.bins + e);
+  __syncthreads();
+  // Kept count per expert, then an inclusive block scan (kPer experts per thread).
+  int32_t kc[kPer];
+  int32_t run = 0;
 #pragma unroll
-      for (int u = 0; u < U; ++u) {
-        const int64_t c = c0 + u * kWarp + lane;
-        if (c < g.vecs) {
-          vx[u] = ld_once(xr + c);  // each expert row is read once
-          vg[u] = BY_ASSIGNMENT ? ld_l1(gv + c) : ld_keep(gv + c);
+  for (int q = 0; q < kPer; ++q) {
+    const int e = tid * kPer + q;
+    int32_t c = 0;
+    if (e < g.E) {
+      const int32_t prev = e > 0 ? sbins[e - 1] : 0;
+      const bool ok = sbins[e] >= prev && (e < g.E - 1 || sbins[e] <= g.n) && prev >= 0;
+      if (!ok && blockIdx.x == 0) flag_status(g.status, MOE_STATUS_BAD_BINS);
+      c = ok ? min(sbins[e] - prev, g.capacity) : 0;
+    }
+    run += c;
+    kc[q] = run;
+  }
+  int32_t incl = run;
+#pragma unroll
+  for (int d = 1; d < kWarp; d <<= 1) {
+    const int32_t v = __shfl_up_sync(kAll, incl, d);
+    if (lane >= d) incl += v;
+  }
+  if (lane == kWarp - 1) swarp[warp] = incl;
+  __syncthreads();
+  int32_t before = incl - run;
+  for (int w = 0; w < warp; ++w) before += swarp[w];
+#pragma unroll
+  for (int q = 0; q < kPer; ++q) {
+    const int e = tid * kPer + q;
+    if (e < g.E) skept[e] = before + kc[q];
+  }
+  __syncthreads();
+
+  // Dropped slots (and slots whose data are inconsistent) get 0.
+  const int64_t threads = (int64_t)gridDim.x * kThreads;
+  for (int64_t i = (int64_t)blockIdx.x * kThreads + tid; i < g.n; i += threads) {
+    const int32_t e = __ldg(g.bin_ids + i);
+    bool zero;
+    if (e < 0 || e >= g.E) {
+      flag_status(g.status, MOE_STATUS_BAD_EXPERT);
+      zero = true;
+    } else {
+      const int64_t start = e > 0 ? sbins[e - 1] : 0;
+      if (i < start || i >= sbins[e]) {
+        flag_status(g.status, MOE_STATUS_BAD_BINS);
+        zero = true;
+      } else {
+        zero = i - start >= g.capacity;
+      }
+    }
+    if (zero) {
+      const int32_t a = __ldg(g.indices + i);
+      if (a >= 0 && a < g.n) g.wgrad[a] = 0.0f;
+      else flag_status(g.status, MOE_STATUS_BAD_INDEX);
+    }
+  }
+
+  const int64_t kept = skept[g.E - 1];
+  const int64_t warps = (int64_t)gridDim.x * (kThreads / kWarp);
+  const int64_t first = (int64_t)blockIdx.x * (kThreads / kWarp) + warp;
+  const V* __restrict__ xe = reinterpret_cast<const V*>(g.xe);
+  const V* __restrict__ gr = reinterpret_cast<const V*>(g.grad);
+  for (int64_t base = first; base < kept; base += kWarp * warps) {
+    const int64_t k = base + lane * warps;
+    int64_t row = -1;
+    int32_t a = -1;
+    if (k < kept) {
+      int lo = 0, hi = g.E - 1;  // first expert whose kept prefix passes k
+      while (lo < hi) {
+        const int mid = (lo + hi) >> 1;
+        if (skept[mid] > k) hi = mid;
+        else lo = mid + 1;
+      }
+      const int64_t j = k - (lo > 0 ? skept[lo - 1] : 0);
+      const int64_t i = (lo > 0 ? sbins[lo - 1] : 0) + j;
+      if (i >= g.n) {
+        flag_status(g.status, MOE_STATUS_BAD_BINS);
+      } else {
+        a = __ldg(g.indices + i);
+        const int32_t e = __ldg(g.bin_ids + i);
+        if (a < 0 || a >= g.n) {
+          flag_status(g.status, MOE_STATUS_BAD_INDEX);
+          a = -1;
+        } else if (e != lo) {
+          flag_status(g.status, MOE_STATUS_BAD_BINS);  // the zero pass wrote this slot
+          a = -1;
+        } else {
+          row = (int64_t)lo * g.capacity + j;
         }
       }
-#pragma unroll
-      for (int u = 0; u < U; ++u) {
-        const int64_t c = c0 + u * kWarp + lane;
-        if (c < g.vecs) {
-          if constexpr (kPacked) {
-#pragma unroll
-            for (int p = 0; p < NE / 2; ++p)
-              acc2[p & 1].add_exact(f2_mul(f2_elems<ET>(vx[u], p), f2_elems<ET>(vg[u], p)));
-          } else {
-#pragma unroll
-            for (int q = 0; q < NE; ++q) acc[q & 1].template add_product<kExact>(L::get(vx[u], q), L::get(vg[u], q));
-          }
-        }
-      }
     }
-    if constexpr (kPacked) {
-      acc2[0].fold_into(acc[0]);
-      acc2[1].fold_into(acc[1]);
+    // The batch waits in shared memory, so its registers are free for the dots.
+    __syncwarp();
+    srow[tid] = row;
+    sa[tid] = a;
+    __syncwarp();
+    const int n_here = (int)min((int64_t)kWarp, (kept - base + warps - 1) / warps);
+    for (int q = 0; q < n_here; ++q) {
+      const int64_t r = srow[warp * kWarp + q];
+      const int32_t aq = sa[warp * kWarp + q];
+      if (r < 0) continue;
+      const float d = row_dot<VB, U, ET, false>(xe + r * g.vecs, gr + (aq / g.top_k) * g.vecs, g.vecs, lane);
+      if (lane == 0) g.wgrad[aq] = d;
     }
-    acc[0].merge(acc[1].s, acc[1].c);
-#pragma unroll
-    for (int d = kWarp / 2; d > 0; d >>= 1) {
-      const float s2 = __shfl_xor_sync(0xffffffffu, acc[0].s, d);
-      const float c2 = __shfl_xor_sync(0xffffffffu, acc[0].c, d);
-      acc[0].merge(s2, c2);
-    }
-    if (lane == 0) g.wgrad[a] = __fadd_rn(acc[0].s, acc[0].c);
   }
 }
 
 // Padded rows hold every assignment (TOP_K per token): assignment order,
 // which reads each gradient row once, measured fastest there. Binned rows
 // hold only the slots within capacity (fewer per token, so fewer gradient
-// re-reads, which L2 catches): sorted order, with its address-ordered row
-// reads, measured fastest there.
+// re-reads, which L2 catches): the kept rows in row order, measured fastest
+// there; with more experts than the shared-memory stage holds, the sorted
+// walk over every position (dropped ones write 0) instead.
+#ifndef MOE_WGRAD_KEPT
+#define MOE_WGRAD_KEPT 1
+#endif
+
 template <int VB, typename ET, bool PADDED>
 int launch_wgrad(const WgradArgs& g, cudaStream_t s) {
   constexpr bool kByAssignment = PADDED;
   if (kByAssignment) {
     const int64_t blocks = (g.n + 255) / 256;
-    launch(positions_kernel, (unsigned)(blocks < 4096 ? blocks : 4096), 256, 0, s, 
+    launch(positions_kernel, (unsigned)(blocks < 4096 ? blocks : 4096), 256, 0, s,
         g.indices, g.n, reinterpret_cast<int32_t*>(g.wgrad), g.status);
     if (check_launch() != MOE_OK) return MOE_ERR_CUDA;
   }
   constexpr int U = VB == 32 ? 2 : (VB == 16 ? 4 : 8);  // 64 bytes per lane and operand in flight
+  if (!PADDED && MOE_WGRAD_KEPT && g.E <= kKeptStage) {
+    auto kk = wgrad_kept_kernel<VB, U, ET>;
+    const int64_t work_ctas = (g.n + (kThreads / kWarp) - 1) / (kThreads / kWarp);  // a warp per slot at most
+    launch(kk, persistent_grid(kk, kThreads, 0, work_ctas), kThreads, 0, s, g);
+    return check_launch();
+  }
   auto k = wgrad_kernel<VB, U, ET, PADDED, kByAssignment>;
   const int64_t work_ctas = (g.n + (kThreads / kWarp) - 1) / (kThreads / kWarp);
   launch(k, persistent_grid(k, kThreads, 0, work_ctas), kThreads, 0, s, g);

@@ -371,6 +371,41 @@ def test_bad_expert_ids_are_reported_not_faulted():
     assert int(st.item()) & _lib.MOE_STATUS_BAD_EXPERT
 
 
+def test_wgrad_reports_corrupt_routing():
+    """Binned wgrad (kept-slot walk and zero pass) and padded wgrad (positions
+    pass and assignment walk) on corrupt routing data: every read is range-
+    checked, so each case sets its status bit instead of faulting."""
+    r = wl.uniform_routing("corrupt-wgrad", 32, 16, 4, 2, wl.F32, capacity=8, pad_multiple=4, seed=13)
+    route = p.moe_route_build(to_dev(r.top_expert, DEV), 4, 4)
+    xe = torch.randn(4, 8, 16, device=DEV)
+    xp = torch.randn(80, 16, device=DEV)  # >= n + E*(m-1) padded rows
+    grad = to_dev(r.grad, DEV)
+    bad_bins = torch.tensor([40, 10, 70, 64], dtype=torch.int32, device=DEV)
+    bad_ids = route.bin_ids.clone()
+    bad_ids[5] = 7
+    bad_idx = route.indices.clone()
+    bad_idx[3] = 1 << 20
+    cases = [
+        ("binned, bins", _lib.MOE_STATUS_BAD_BINS,
+         lambda st: p.moe_binned_wgrad(xe, grad, route.indices, route.bin_ids, bad_bins, 2, status=st)),
+        ("binned, expert id", _lib.MOE_STATUS_BAD_EXPERT,
+         lambda st: p.moe_binned_wgrad(xe, grad, route.indices, bad_ids, route.bins, 2, status=st)),
+        ("binned, index", _lib.MOE_STATUS_BAD_INDEX,
+         lambda st: p.moe_binned_wgrad(xe, grad, bad_idx, route.bin_ids, route.bins, 2, status=st)),
+        ("padded, index", _lib.MOE_STATUS_BAD_INDEX,
+         lambda st: p.moe_padded_wgrad(xp, grad, bad_idx, route.bin_ids, route.bins, route.padded_bins, 2,
+                                       status=st)),
+        ("padded, expert id", _lib.MOE_STATUS_BAD_EXPERT,
+         lambda st: p.moe_padded_wgrad(xp, grad, route.indices, bad_ids, route.bins, route.padded_bins, 2,
+                                       status=st)),
+    ]
+    for what, bit, run in cases:
+        st = status_word()
+        run(st)
+        torch.cuda.synchronize()
+        assert int(st.item()) & bit, what
+
+
 def test_corrupt_bins_and_positions_are_reported():
     r = wl.uniform_routing("corrupt", 32, 16, 4, 2, wl.F32, capacity=8, pad_multiple=4, seed=12)
     route = p.moe_route_build(to_dev(r.top_expert, DEV), 4, 4)

@@ -112,10 +112,11 @@ def traffic_from_profiles(kernel: str, digest: str):
 
 
 def l2_flush(buf) -> None:
-    """Evicts L2 before a timed launch: writes `buf` (512 MB, four times
-    L2), then reads it back, so that the dirty lines of the write are
-    written back here rather than inside the next timed kernel. L2 is left
-    holding only clean lines of `buf`, none of the routing data."""
+    """Evicts L2 before a timed launch: writes `buf` (512 MB of fp32, four
+    times L2), then reads it back in place (an fp32 sum makes no widened
+    temporary copy), so that the dirty lines of the write are written back
+    here rather than inside the next timed kernel. L2 is left holding only
+    clean lines of `buf`, none of the routing data."""
     buf.zero_()
     buf.sum()
 
@@ -377,7 +378,7 @@ def run_gpu(args, rank, world, local_rank):
     r, d = rank_workload(rank)
     path = Path(r, d, dev)
     ops = path.ops()
-    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.int32, device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream(dev)
 
     def barrier():

@@ -278,10 +278,13 @@ def test_one_token_and_ragged_chunks():
     run_routing(wl.zipf_routing("ragged", 2053, 16, 64, 3, wl.BF16, capacity=50, pad_multiple=32, seed=8))
 
 
-def test_more_experts_than_staged_bins():
-    # E above the 1024 experts whose bins the kernels stage in shared memory:
-    # bins and padded_bins are read from global memory instead
-    r = wl.zipf_routing("e3000", 700, 24, 3000, 4, wl.BF16, capacity=2, pad_multiple=4, seed=13)
+@pytest.mark.parametrize("E", [1024, 1025, 3000])
+def test_more_experts_than_staged_bins(E):
+    # Around and above the 1024 experts whose bins the kernels stage in
+    # shared memory: above it bins and padded_bins are read from global
+    # memory, and the binned wgrad walks every sorted position instead of
+    # the kept rows only.
+    r = wl.zipf_routing("e%d" % E, 700, 24, E, 4, wl.BF16, capacity=2, pad_multiple=4, seed=13)
     run_routing(r)
     run_fused(r)
 

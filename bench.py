@@ -215,19 +215,19 @@ class Path:
             ("compaction_fwd", 1, lambda: p.moe_routing_map_to_indices_fwd(self.probs, self.rmap, K,
                                                                            out=(self.pi, self.idx))),
             ("route_build", 3, lambda: p.moe_route_build(self.idx, E, r.pad_multiple, workspace=self.ws, out=rt)),
-            ("binned_gather", 3, lambda: p.moe_binned_gather(self.x, rt.indices, rt.bins, E, r.capacity, K,
-                                                             out=self.xb)),
+            ("binned_gather", 1, lambda: p.moe_binned_gather(self.x, rt.indices, rt.bins, E, r.capacity, K,
+                                                             out=self.xb, positions=rt.positions)),
             ("binned_scatter", 1, lambda: p.moe_binned_scatter(self.xb, rt.indices, rt.bin_ids, rt.bins, w, T, K,
                                                                positions=rt.positions, out=self.yb)),
             ("binned_wgrad", 1, lambda: p.moe_binned_wgrad(self.xb, self.grad, rt.indices, rt.bin_ids, rt.bins, K,
                                                            out=self.wgb)),
-            ("padded_gather", 3, lambda: p.moe_padded_gather(self.x, rt.indices, rt.bins, rt.padded_bins, K,
-                                                             out_rows=self.P, out=self.xp)),
+            ("padded_gather", 1, lambda: p.moe_padded_gather(self.x, rt.indices, rt.bins, rt.padded_bins, K,
+                                                             out_rows=self.P, out=self.xp, positions=rt.positions)),
             ("padded_scatter", 1, lambda: p.moe_padded_scatter(self.xp, rt.indices, rt.bin_ids, rt.bins,
                                                                rt.padded_bins, w, T, K, positions=rt.positions,
                                                                out=self.yp)),
-            ("padded_wgrad", 2, lambda: p.moe_padded_wgrad(self.xp, self.grad, rt.indices, rt.bin_ids, rt.bins,
-                                                           rt.padded_bins, K, out=self.wgp)),
+            ("padded_wgrad", 1, lambda: p.moe_padded_wgrad(self.xp, self.grad, rt.indices, rt.bin_ids, rt.bins,
+                                                           rt.padded_bins, K, out=self.wgp, positions=rt.positions)),
             ("compaction_bwd", 1, lambda: p.moe_routing_map_to_indices_bwd(self.wgp.view(T, K), self.idx, E,
                                                                            out=self.gprobs)),
         ]
@@ -254,11 +254,12 @@ class Path:
             ("topk_gating", lambda: p.moe_topk_gating(self.logits, K, "sigmoid", True, out=self.g_out),
              T * E * 4 + T * K * 8),
             ("binned_gather_weighted",
-             lambda: p.moe_binned_gather_weighted(self.grad, rt.indices, rt.bins, w, E, r.capacity, K, out=self.gwb),
+             lambda: p.moe_binned_gather_weighted(self.grad, rt.indices, rt.bins, w, E, r.capacity, K, out=self.gwb,
+                                                  positions=rt.positions),
              self.kept_tokens * H * b + E * r.capacity * H * b + 8 * n + 4 * E),
             ("padded_gather_weighted",
              lambda: p.moe_padded_gather_weighted(self.grad, rt.indices, rt.bins, rt.padded_bins, w, K,
-                                                  out_rows=self.P, out=self.gwp),
+                                                  out_rows=self.P, out=self.gwp, positions=rt.positions),
              T * H * b + self.P * H * b + 8 * n + 8 * E),
             ("route_build_binned_gather",
              lambda: p.moe_route_build_binned_gather(self.idx, self.x, E, r.capacity, r.pad_multiple,
@@ -563,7 +564,8 @@ def time_sweeps(args, path, flush, stream) -> dict:
         kept = int(np.minimum(path.counts, cap).sum())
         xb = torch.empty((E, cap, H), dtype=bf, device=dev)
         ops = [
-            ("binned_gather", lambda: p.moe_binned_gather(path.x, rt.indices, rt.bins, E, cap, K, out=xb),
+            ("binned_gather", lambda: p.moe_binned_gather(path.x, rt.indices, rt.bins, E, cap, K, out=xb,
+                                                          positions=rt.positions),
              path.tokens_with_kept_slot(cap) * H * b + E * cap * H * b + 4 * n + 4 * E),
             ("binned_scatter", lambda: p.moe_binned_scatter(xb, rt.indices, rt.bin_ids, rt.bins, w, T, K,
                                                             positions=rt.positions, out=y),
@@ -582,13 +584,13 @@ def time_sweeps(args, path, flush, stream) -> dict:
         xp = torch.empty((P, H), dtype=bf, device=dev)
         ops = [
             ("padded_gather", lambda: p.moe_padded_gather(path.x, rm.indices, rm.bins, rm.padded_bins, K,
-                                                          out_rows=P, out=xp),
+                                                          out_rows=P, out=xp, positions=rm.positions),
              T * H * b + P * H * b + 4 * n + 8 * E),
             ("padded_scatter", lambda: p.moe_padded_scatter(xp, rm.indices, rm.bin_ids, rm.bins, rm.padded_bins, w,
                                                             T, K, positions=rm.positions, out=y),
              n * H * b + T * H * b + 12 * n + 8 * E),
             ("padded_wgrad", lambda: p.moe_padded_wgrad(xp, path.grad, rm.indices, rm.bin_ids, rm.bins,
-                                                        rm.padded_bins, K, out=wg),
+                                                        rm.padded_bins, K, out=wg, positions=rm.positions),
              n * H * b + T * H * b + 12 * n + 8 * E)]
         pads[str(m)] = {"padded_rows": P}
         pads[str(m)].update({name: time_alone(args, fn, nb, flush, stream) for name, fn, nb in ops})
@@ -639,12 +641,13 @@ def run_e2e(args, path, dev, dist):
         rt, xp = p.moe_route_build_padded_gather(idx, din["x"], E, r.pad_multiple, out_rows=p_max,
                                                  workspace=path.ws)
         w = pi.view(-1)
-        xb = p.moe_binned_gather(din["x"], rt.indices, rt.bins, E, r.capacity, K)
+        xb = p.moe_binned_gather(din["x"], rt.indices, rt.bins, E, r.capacity, K, positions=rt.positions)
         yb = p.moe_binned_scatter(xb, rt.indices, rt.bin_ids, rt.bins, w, T, K, positions=rt.positions)
         p.moe_binned_wgrad(xb, din["grad"], rt.indices, rt.bin_ids, rt.bins, K)
         yp = p.moe_padded_scatter(xp, rt.indices, rt.bin_ids, rt.bins, rt.padded_bins, w, T, K,
                                   positions=rt.positions)
-        wgp = p.moe_padded_wgrad(xp, din["grad"], rt.indices, rt.bin_ids, rt.bins, rt.padded_bins, K)
+        wgp = p.moe_padded_wgrad(xp, din["grad"], rt.indices, rt.bin_ids, rt.bins, rt.padded_bins, K,
+                                 positions=rt.positions)
         gp = p.moe_routing_map_to_indices_bwd(wgp.view(T, K), idx, E)
         ev_used[b].record(sc)
         s_out.wait_event(ev_used[b])

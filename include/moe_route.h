@@ -179,20 +179,26 @@ int moe_check_routing(const int32_t* indices, const int32_t* bin_ids,
  * with bins[-1] read as 0. Assignments beyond capacity are dropped.
  *   x    [T, H] dtype;  out [E, capacity, H] dtype (fully written).
  *   indices [n], bins [E] from moe_route_build; n = T*top_k.
+ *   positions [n] int32, nullable: the inverse permutation of indices
+ *   (positions[indices[i]] = i), as moe_route_build writes it. Every entry
+ *   is checked against indices before it is followed.
  * capacity >= 0; capacity == 0 writes nothing.
- * Schedule (the result does not depend on it): when out holds more than
- * 4n bytes plus one row, the gather first stores the inverse permutation of
- * indices in the last 4n bytes of out (16-byte aligned), then copies each
- * token row once to all of its kept rows, then writes the rows that overlap
- * those bytes; three launches, no workspace. out must not alias any input.
+ * Schedule (the result does not depend on it): with positions, one launch
+ * that copies each token row once to all of its kept rows and zero-fills
+ * the rest. Without them, when out holds more than 4n bytes plus one row,
+ * the gather first stores the inverse permutation of indices in the last 4n
+ * bytes of out (16-byte aligned), then copies each token row once to all of
+ * its kept rows, then writes the rows that overlap those bytes; three
+ * launches, no workspace. out must not alias any input.
  * A sorted position that does not map back to its assignment (indices not a
  * permutation) sets MOE_STATUS_BAD_INDEX; bins that decrease or pass n set
  * MOE_STATUS_BAD_BINS. The same holds for every gather below.
  */
 int moe_binned_gather(const void* x, int32_t dtype, const int32_t* indices,
-                      const int32_t* bins, int64_t num_tokens, int64_t hidden,
-                      int32_t num_experts, int32_t capacity, int32_t top_k,
-                      void* out, int32_t* d_status, moe_stream_t stream);
+                      const int32_t* bins, const int32_t* positions,
+                      int64_t num_tokens, int64_t hidden, int32_t num_experts,
+                      int32_t capacity, int32_t top_k, void* out,
+                      int32_t* d_status, moe_stream_t stream);
 
 /*
  * Padded gather ([padded] Goal, Workflow steps 4-5, Implementation Pattern,
@@ -206,9 +212,10 @@ int moe_binned_gather(const void* x, int32_t dtype, const int32_t* indices,
  */
 int moe_padded_gather(const void* x, int32_t dtype, const int32_t* indices,
                       const int32_t* bins, const int32_t* padded_bins,
-                      int64_t num_tokens, int64_t hidden, int32_t num_experts,
-                      int32_t top_k, void* out, int64_t out_rows,
-                      int32_t* d_status, moe_stream_t stream);
+                      const int32_t* positions, int64_t num_tokens,
+                      int64_t hidden, int32_t num_experts, int32_t top_k,
+                      void* out, int64_t out_rows, int32_t* d_status,
+                      moe_stream_t stream);
 
 /*
  * Weighted gather: the gradient of the combine (moe_*_scatter with weights)
@@ -224,17 +231,18 @@ int moe_padded_gather(const void* x, int32_t dtype, const int32_t* indices,
  */
 int moe_binned_gather_weighted(const void* dy, int32_t dtype,
                                const int32_t* indices, const int32_t* bins,
-                               const float* weights, int64_t num_tokens,
-                               int64_t hidden, int32_t num_experts,
-                               int32_t capacity, int32_t top_k, void* out,
-                               int32_t* d_status, moe_stream_t stream);
+                               const float* weights, const int32_t* positions,
+                               int64_t num_tokens, int64_t hidden,
+                               int32_t num_experts, int32_t capacity,
+                               int32_t top_k, void* out, int32_t* d_status,
+                               moe_stream_t stream);
 int moe_padded_gather_weighted(const void* dy, int32_t dtype,
                                const int32_t* indices, const int32_t* bins,
                                const int32_t* padded_bins, const float* weights,
-                               int64_t num_tokens, int64_t hidden,
-                               int32_t num_experts, int32_t top_k, void* out,
-                               int64_t out_rows, int32_t* d_status,
-                               moe_stream_t stream);
+                               const int32_t* positions, int64_t num_tokens,
+                               int64_t hidden, int32_t num_experts,
+                               int32_t top_k, void* out, int64_t out_rows,
+                               int32_t* d_status, moe_stream_t stream);
 
 /*
  * Route build and gather in one call ([padded] Workflow steps 1-5;
@@ -317,10 +325,12 @@ int moe_padded_scatter(const void* xe, int32_t dtype, const int32_t* indices,
  * Accumulated in fp32 with compensated (error-free transformation)
  * summation, so the result is close to the correctly rounded dot.
  *   xe as for scatter; grad [T, H] dtype; wgrad [n] fp32 (fully written).
- * No workspace. moe_padded_wgrad takes two launches: the first stores the
- * inverse permutation of indices in wgrad itself (n 32-bit slots), the
- * second reads each slot once and overwrites it with the result, visiting
- * assignments in id order so that each gradient row is read about once.
+ * No workspace. moe_padded_wgrad visits assignments in id order so that
+ * each gradient row is read about once; it takes positions (nullable, the
+ * inverse permutation of indices as moe_route_build writes it, each entry
+ * checked against indices): with them, one launch; without them, two (the
+ * first stores the inverse permutation in wgrad itself, n 32-bit slots, the
+ * second reads each slot once and overwrites it with the result).
  * moe_binned_wgrad is one launch: for E <= 1024 its warps visit only the
  * kept rows (a thread per sorted position writes the dropped slots' 0),
  * otherwise every sorted position. wgrad must not
@@ -337,9 +347,10 @@ int moe_binned_wgrad(const void* xe, const void* grad, int32_t dtype,
 int moe_padded_wgrad(const void* xe, const void* grad, int32_t dtype,
                      const int32_t* indices, const int32_t* bin_ids,
                      const int32_t* bins, const int32_t* padded_bins,
-                     int64_t num_tokens, int64_t hidden, int32_t num_experts,
-                     int32_t top_k, int64_t xe_rows, float* wgrad,
-                     int32_t* d_status, moe_stream_t stream);
+                     const int32_t* positions, int64_t num_tokens,
+                     int64_t hidden, int32_t num_experts, int32_t top_k,
+                     int64_t xe_rows, float* wgrad, int32_t* d_status,
+                     moe_stream_t stream);
 
 /*
  * Router top-k gating: the step before the route build ("Fused MoE Dispatch

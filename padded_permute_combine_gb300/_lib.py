@@ -35,11 +35,12 @@ SIGNATURES = {
     "moe_route_build": (ctypes.c_int, [_P, _I64, _I32, _I32, _P, _P, _P, _P, _P, _P, _SZ, _P, _P]),
     "moe_route_build_noalloc": (ctypes.c_int, [_P, _I64, _I32, _I32, _P, _P, _P, _P, _P, _P, _P]),
     "moe_check_routing": (ctypes.c_int, [_P, _P, _P, _P, _P, _I64, _I32, _P, _P]),
-    "moe_binned_gather": (ctypes.c_int, [_P, _I32, _P, _P, _I64, _I64, _I32, _I32, _I32, _P, _P, _P]),
-    "moe_padded_gather": (ctypes.c_int, [_P, _I32, _P, _P, _P, _I64, _I64, _I32, _I32, _P, _I64, _P, _P]),
-    "moe_binned_gather_weighted": (ctypes.c_int, [_P, _I32, _P, _P, _P, _I64, _I64, _I32, _I32, _I32, _P, _P, _P]),
-    "moe_padded_gather_weighted": (ctypes.c_int, [_P, _I32, _P, _P, _P, _P, _I64, _I64, _I32, _I32, _P, _I64, _P,
+    "moe_binned_gather": (ctypes.c_int, [_P, _I32, _P, _P, _P, _I64, _I64, _I32, _I32, _I32, _P, _P, _P]),
+    "moe_padded_gather": (ctypes.c_int, [_P, _I32, _P, _P, _P, _P, _I64, _I64, _I32, _I32, _P, _I64, _P, _P]),
+    "moe_binned_gather_weighted": (ctypes.c_int, [_P, _I32, _P, _P, _P, _P, _I64, _I64, _I32, _I32, _I32, _P, _P,
                                                   _P]),
+    "moe_padded_gather_weighted": (ctypes.c_int, [_P, _I32, _P, _P, _P, _P, _P, _I64, _I64, _I32, _I32, _P, _I64,
+                                                  _P, _P]),
     "moe_route_build_binned_gather": (ctypes.c_int, [_P, _P, _I32, _I64, _I64, _I32, _I32, _I32, _I32, _P, _P, _P,
                                                      _P, _P, _P, _P, _SZ, _P, _P]),
     "moe_route_build_padded_gather": (ctypes.c_int, [_P, _P, _I32, _I64, _I64, _I32, _I32, _I32, _P, _P, _P, _P,
@@ -50,7 +51,8 @@ SIGNATURES = {
     "moe_padded_scatter": (ctypes.c_int, [_P, _I32, _P, _P, _P, _P, _P, _P, _I64, _I64, _I32, _I32, _I64, _P, _P,
                                           _SZ, _P, _P]),
     "moe_binned_wgrad": (ctypes.c_int, [_P, _P, _I32, _P, _P, _P, _I64, _I64, _I32, _I32, _I32, _P, _P, _P]),
-    "moe_padded_wgrad": (ctypes.c_int, [_P, _P, _I32, _P, _P, _P, _P, _I64, _I64, _I32, _I32, _I64, _P, _P, _P]),
+    "moe_padded_wgrad": (ctypes.c_int, [_P, _P, _I32, _P, _P, _P, _P, _P, _I64, _I64, _I32, _I32, _I64, _P, _P,
+                                        _P]),
     "moe_topk_gating": (ctypes.c_int, [_P, _I64, _I32, _I32, _I32, _I32, _P, _P, _P]),
     "moe_routing_map_to_indices_fwd": (ctypes.c_int, [_P, _P, _I64, _I32, _I32, _P, _P, _P]),
     "moe_routing_map_to_indices_bwd": (ctypes.c_int, [_P, _P, _I64, _I32, _I32, _P, _P, _P]),

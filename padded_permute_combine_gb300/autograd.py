@@ -58,8 +58,10 @@ class Permute(torch.autograd.Function):
         x = x.detach().contiguous()
         ctx.route, ctx.top_k, ctx.num_tokens, ctx.capacity = route, top_k, x.shape[0], capacity
         if capacity is not None:
-            return ops.moe_binned_gather(x, route.indices, route.bins, num_experts, capacity, top_k)
-        return ops.moe_padded_gather(x, route.indices, route.bins, route.padded_bins, top_k)
+            return ops.moe_binned_gather(x, route.indices, route.bins, num_experts, capacity, top_k,
+                                         positions=route.positions)
+        return ops.moe_padded_gather(x, route.indices, route.bins, route.padded_bins, top_k,
+                                     positions=route.positions)
 
     @staticmethod
     def backward(ctx, grad_xe):
@@ -96,13 +98,15 @@ class Combine(torch.autograd.Function):
         if ctx.padded:
             if ctx.needs_input_grad[0]:
                 dxe = ops.moe_padded_gather_weighted(dy, r.indices, r.bins, r.padded_bins, w, K,
-                                                     out_rows=xe.shape[0])
+                                                     out_rows=xe.shape[0], positions=r.positions)
             if ctx.needs_input_grad[1]:
-                dw = ops.moe_padded_wgrad(xe, dy, r.indices, r.bin_ids, r.bins, r.padded_bins, K)
+                dw = ops.moe_padded_wgrad(xe, dy, r.indices, r.bin_ids, r.bins, r.padded_bins, K,
+                                          positions=r.positions)
         else:
             E, capacity = xe.shape[0], xe.shape[1]
             if ctx.needs_input_grad[0]:
-                dxe = ops.moe_binned_gather_weighted(dy, r.indices, r.bins, w, E, capacity, K)
+                dxe = ops.moe_binned_gather_weighted(dy, r.indices, r.bins, w, E, capacity, K,
+                                                     positions=r.positions)
             if ctx.needs_input_grad[1]:
                 dw = ops.moe_binned_wgrad(xe, dy, r.indices, r.bin_ids, r.bins, K)
         return dxe, None if dw is None else dw.view(ctx.w_shape), None, None, None, None

@@ -49,7 +49,7 @@ struct GatherArgs {
   int32_t* status;
   int64_t T = 0;
   int64_t row_begin = 0;              // first row the destination-major kernel writes
-  const int32_t* positions = nullptr;  // token-major path: inverse of indices, in the tail of out
+  const int32_t* positions = nullptr;  // token-major path: inverse of indices (the caller's, or in the tail of out)
   int64_t segs = 1;      // token-major path: work items per token (column segments of its row)
   int64_t seg_len = 0;   // vectors (register pass) or bytes (bulk-copy pass) per segment
 };
@@ -541,7 +541,7 @@ int launch_gather(GatherArgs g, int64_t row_bytes, cudaStream_t s) {
   g.seg_len = ((g.vecs + g.segs - 1) / g.segs + kWarp - 1) / kWarp * kWarp;  // vectors, whole warp passes
   g.segs = g.seg_len > 0 ? (g.vecs + g.seg_len - 1) / g.seg_len : 1;
   if (g.positions != nullptr) {
-    // The caller's positions (route build in the same call): one token pass over every row.
+    // The caller's positions (from its route build): one token pass over every row.
     g.row_begin = g.rows_out;
     int rc = MOE_OK;
     if (std::is_void<ST>::value && launch_gather_tma<PADDED>(g, row_bytes, s, &rc)) return rc;
@@ -621,10 +621,11 @@ int gather_checks(const void* x, int32_t dtype, const int32_t* indices, const in
 using namespace moe;
 
 extern "C" int moe_binned_gather(const void* x, int32_t dtype, const int32_t* indices, const int32_t* bins,
-                                 int64_t T, int64_t H, int32_t E, int32_t capacity, int32_t top_k, void* out,
-                                 int32_t* d_status, moe_stream_t stream) {
+                                 const int32_t* positions, int64_t T, int64_t H, int32_t E, int32_t capacity,
+                                 int32_t top_k, void* out, int32_t* d_status, moe_stream_t stream) {
   const int rc = gather_checks(x, dtype, indices, bins, T, H, E, top_k, out, d_status);
   if (rc != MOE_OK) return rc;
+  if (positions != nullptr && !aligned(positions, 4)) return MOE_ERR_UNSUPPORTED;
   if (capacity < 0) return MOE_ERR_INVALID_ARG;
   const int64_t rows = (int64_t)E * capacity;
   if (rows == 0 || H == 0) return MOE_OK;
@@ -632,31 +633,36 @@ extern "C" int moe_binned_gather(const void* x, int32_t dtype, const int32_t* in
   GatherArgs g{static_cast<const char*>(x), static_cast<char*>(out), indices, bins, nullptr, nullptr, T * top_k,
                rows, H, E, capacity, top_k, d_status};
   g.T = T;
+  g.positions = positions;
   return dispatch_gather<false>(g, dtype, reinterpret_cast<cudaStream_t>(stream));
 }
 
 extern "C" int moe_padded_gather(const void* x, int32_t dtype, const int32_t* indices, const int32_t* bins,
-                                 const int32_t* padded_bins, int64_t T, int64_t H, int32_t E, int32_t top_k,
-                                 void* out, int64_t out_rows, int32_t* d_status, moe_stream_t stream) {
+                                 const int32_t* padded_bins, const int32_t* positions, int64_t T, int64_t H,
+                                 int32_t E, int32_t top_k, void* out, int64_t out_rows, int32_t* d_status,
+                                 moe_stream_t stream) {
   const int rc = gather_checks(x, dtype, indices, bins, T, H, E, top_k, out, d_status);
   if (rc != MOE_OK) return rc;
   if (padded_bins == nullptr || out_rows < 0) return MOE_ERR_INVALID_ARG;
-  if (!aligned(padded_bins, 4)) return MOE_ERR_UNSUPPORTED;
+  if (!aligned(padded_bins, 4) || (positions != nullptr && !aligned(positions, 4))) return MOE_ERR_UNSUPPORTED;
   if (out_rows == 0 || H == 0) return MOE_OK;
   if (out == nullptr) return MOE_ERR_INVALID_ARG;
   GatherArgs g{static_cast<const char*>(x), static_cast<char*>(out), indices, bins, padded_bins, nullptr, T * top_k,
                out_rows, H, E, 0, top_k, d_status};
   g.T = T;
+  g.positions = positions;
   return dispatch_gather<true>(g, dtype, reinterpret_cast<cudaStream_t>(stream));
 }
 
 extern "C" int moe_binned_gather_weighted(const void* dy, int32_t dtype, const int32_t* indices, const int32_t* bins,
-                                          const float* weights, int64_t T, int64_t H, int32_t E, int32_t capacity,
-                                          int32_t top_k, void* out, int32_t* d_status, moe_stream_t stream) {
+                                          const float* weights, const int32_t* positions, int64_t T, int64_t H,
+                                          int32_t E, int32_t capacity, int32_t top_k, void* out, int32_t* d_status,
+                                          moe_stream_t stream) {
   const int rc = gather_checks(dy, dtype, indices, bins, T, H, E, top_k, out, d_status);
   if (rc != MOE_OK) return rc;
   if (capacity < 0) return MOE_ERR_INVALID_ARG;
-  if (weights != nullptr && !aligned(weights, 4)) return MOE_ERR_UNSUPPORTED;
+  if ((weights != nullptr && !aligned(weights, 4)) || (positions != nullptr && !aligned(positions, 4)))
+    return MOE_ERR_UNSUPPORTED;
   if (T > 0 && weights == nullptr) return MOE_ERR_INVALID_ARG;
   const int64_t rows = (int64_t)E * capacity;
   if (rows == 0 || H == 0) return MOE_OK;
@@ -664,23 +670,27 @@ extern "C" int moe_binned_gather_weighted(const void* dy, int32_t dtype, const i
   GatherArgs g{static_cast<const char*>(dy), static_cast<char*>(out), indices, bins, nullptr, weights, T * top_k,
                rows, H, E, capacity, top_k, d_status};
   g.T = T;
+  g.positions = positions;
   return dispatch_gather<false>(g, dtype, reinterpret_cast<cudaStream_t>(stream));
 }
 
 extern "C" int moe_padded_gather_weighted(const void* dy, int32_t dtype, const int32_t* indices, const int32_t* bins,
-                                          const int32_t* padded_bins, const float* weights, int64_t T, int64_t H,
-                                          int32_t E, int32_t top_k, void* out, int64_t out_rows, int32_t* d_status,
-                                          moe_stream_t stream) {
+                                          const int32_t* padded_bins, const float* weights,
+                                          const int32_t* positions, int64_t T, int64_t H, int32_t E, int32_t top_k,
+                                          void* out, int64_t out_rows, int32_t* d_status, moe_stream_t stream) {
   const int rc = gather_checks(dy, dtype, indices, bins, T, H, E, top_k, out, d_status);
   if (rc != MOE_OK) return rc;
   if (padded_bins == nullptr || out_rows < 0) return MOE_ERR_INVALID_ARG;
-  if (!aligned(padded_bins, 4) || (weights != nullptr && !aligned(weights, 4))) return MOE_ERR_UNSUPPORTED;
+  if (!aligned(padded_bins, 4) || (weights != nullptr && !aligned(weights, 4)) ||
+      (positions != nullptr && !aligned(positions, 4)))
+    return MOE_ERR_UNSUPPORTED;
   if (T > 0 && weights == nullptr) return MOE_ERR_INVALID_ARG;
   if (out_rows == 0 || H == 0) return MOE_OK;
   if (out == nullptr) return MOE_ERR_INVALID_ARG;
   GatherArgs g{static_cast<const char*>(dy), static_cast<char*>(out), indices, bins, padded_bins, weights,
                T * top_k, out_rows, H, E, 0, top_k, d_status};
   g.T = T;
+  g.positions = positions;
   return dispatch_gather<true>(g, dtype, reinterpret_cast<cudaStream_t>(stream));
 }
 

@@ -48,6 +48,7 @@ struct WgradArgs {
   int32_t capacity;
   int32_t top_k;
   int32_t* status;
+  const int32_t* positions = nullptr;  // padded: the caller's inverse of indices (else built in wgrad)
 };
 
 // Running compensated sum: value s plus accumulated rounding errors c.
@@ -148,7 +149,8 @@ __device__ __forceinline__ int64_t expert_row(const WgradArgs& g, int64_t i, int
 // permutation) is caught rather than followed.
 template <bool PADDED>
 __device__ __forceinline__ int64_t assignment_row(const WgradArgs& g, int64_t a) {
-  const int32_t i = ld_position(reinterpret_cast<const int32_t*>(g.wgrad) + a);
+  const int32_t i = g.positions != nullptr ? __ldg(g.positions + a)
+                                            : ld_position(reinterpret_cast<const int32_t*>(g.wgrad) + a);
   if (i < 0 || i >= g.n) {
     flag_status(g.status, MOE_STATUS_BAD_INDEX);
     return -1;
@@ -416,7 +418,7 @@ __global__ void __launch_bounds__(kThreads, 4) wgrad_kept_kernel(WgradArgs g) {
 template <int VB, typename ET, bool PADDED>
 int launch_wgrad(const WgradArgs& g, cudaStream_t s) {
   constexpr bool kByAssignment = PADDED;
-  if (kByAssignment) {
+  if (kByAssignment && g.positions == nullptr) {
     const int64_t blocks = (g.n + 255) / 256;
     launch(positions_kernel, (unsigned)(blocks < 4096 ? blocks : 4096), 256, 0, s,
         g.indices, g.n, reinterpret_cast<int32_t*>(g.wgrad), g.status);
@@ -498,16 +500,17 @@ extern "C" int moe_binned_wgrad(const void* xe, const void* grad, int32_t dtype,
 }
 
 extern "C" int moe_padded_wgrad(const void* xe, const void* grad, int32_t dtype, const int32_t* indices,
-                                const int32_t* bin_ids, const int32_t* bins, const int32_t* padded_bins, int64_t T,
-                                int64_t H, int32_t E, int32_t top_k, int64_t xe_rows, float* wgrad,
-                                int32_t* d_status, moe_stream_t stream) {
+                                const int32_t* bin_ids, const int32_t* bins, const int32_t* padded_bins,
+                                const int32_t* positions, int64_t T, int64_t H, int32_t E, int32_t top_k,
+                                int64_t xe_rows, float* wgrad, int32_t* d_status, moe_stream_t stream) {
   const int rc = wgrad_checks(xe, grad, dtype, indices, bin_ids, bins, T, H, E, top_k, wgrad, d_status);
   if (rc != MOE_OK) return rc;
   if (padded_bins == nullptr || xe_rows < 0) return MOE_ERR_INVALID_ARG;
-  if (!aligned(padded_bins, 4)) return MOE_ERR_UNSUPPORTED;
+  if (!aligned(padded_bins, 4) || (positions != nullptr && !aligned(positions, 4))) return MOE_ERR_UNSUPPORTED;
   if (T == 0) return MOE_OK;
   if (xe == nullptr && xe_rows > 0 && H > 0) return MOE_ERR_INVALID_ARG;
   WgradArgs g{static_cast<const char*>(xe), static_cast<const char*>(grad), wgrad, indices, bin_ids, bins,
               padded_bins, T, T * top_k, H, xe_rows, E, 0, top_k, d_status};
+  g.positions = positions;
   return run_wgrad<true>(g, dtype, reinterpret_cast<cudaStream_t>(stream));
 }

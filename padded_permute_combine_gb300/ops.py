@@ -26,6 +26,11 @@ def _ptr(t: torch.Tensor | None) -> int | None:
     return None if t is None else t.data_ptr()
 
 
+def _need_numel(t: torch.Tensor, n: int, name: str) -> None:
+    if t.numel() != n:
+        raise ValueError("%s must have %d elements, has %d" % (name, n, t.numel()))
+
+
 def _need(t: torch.Tensor, dtype: torch.dtype | None, name: str, device=None) -> torch.Tensor:
     if not isinstance(t, torch.Tensor):
         raise TypeError("%s must be a torch.Tensor" % name)
@@ -101,45 +106,55 @@ def moe_check_routing(indices: torch.Tensor, bin_ids: torch.Tensor, bins: torch.
 
 def moe_binned_gather(x: torch.Tensor, indices: torch.Tensor, bins: torch.Tensor, num_experts: int,
                       capacity: int, top_k: int, out: torch.Tensor | None = None,
-                      status: torch.Tensor | None = None) -> torch.Tensor:
-    """x [T, H] -> [E, capacity, H]; overflow dropped, unused rows zero."""
+                      status: torch.Tensor | None = None, positions: torch.Tensor | None = None) -> torch.Tensor:
+    """x [T, H] -> [E, capacity, H]; overflow dropped, unused rows zero.
+    ``positions``: the route build's inverse permutation of indices (saves
+    the gather rebuilding it)."""
     _need(x, None, "x")
     dt = _act_dtype(x, "x")
     T, H = x.shape
     _need(indices, torch.int32, "indices", x.device)
     _need(bins, torch.int32, "bins", x.device)
+    if positions is not None:
+        _need(positions, torch.int32, "positions", x.device)
+        _need_numel(positions, T * top_k, "positions")
     if out is None:
         out = torch.empty((num_experts, capacity, H), dtype=x.dtype, device=x.device)
     _need(out, x.dtype, "out", x.device)
-    _lib.call("moe_binned_gather", _ptr(x), dt, _ptr(indices), _ptr(bins), T, H, num_experts, capacity, top_k,
-              _ptr(out), _ptr(status), _stream(x))
+    _lib.call("moe_binned_gather", _ptr(x), dt, _ptr(indices), _ptr(bins), _ptr(positions), T, H, num_experts,
+              capacity, top_k, _ptr(out), _ptr(status), _stream(x))
     return out
 
 
 def moe_padded_gather(x: torch.Tensor, indices: torch.Tensor, bins: torch.Tensor, padded_bins: torch.Tensor,
                       top_k: int, out_rows: int | None = None, out: torch.Tensor | None = None,
-                      status: torch.Tensor | None = None) -> torch.Tensor:
+                      status: torch.Tensor | None = None, positions: torch.Tensor | None = None) -> torch.Tensor:
     """x [T, H] -> [padded_bins[-1], H]; padding rows zero. ``out_rows``
-    defaults to padded_bins[-1], read back from the device."""
+    defaults to padded_bins[-1], read back from the device. ``positions`` as
+    for moe_binned_gather."""
     _need(x, None, "x")
     dt = _act_dtype(x, "x")
     T, H = x.shape
     _need(indices, torch.int32, "indices", x.device)
     _need(bins, torch.int32, "bins", x.device)
     _need(padded_bins, torch.int32, "padded_bins", x.device)
+    if positions is not None:
+        _need(positions, torch.int32, "positions", x.device)
+        _need_numel(positions, T * top_k, "positions")
     if out_rows is None:
         out_rows = int(padded_bins[-1].item()) if out is None else out.shape[0]
     if out is None:
         out = torch.empty((out_rows, H), dtype=x.dtype, device=x.device)
     _need(out, x.dtype, "out", x.device)
-    _lib.call("moe_padded_gather", _ptr(x), dt, _ptr(indices), _ptr(bins), _ptr(padded_bins), T, H,
-              padded_bins.numel(), top_k, _ptr(out), out_rows, _ptr(status), _stream(x))
+    _lib.call("moe_padded_gather", _ptr(x), dt, _ptr(indices), _ptr(bins), _ptr(padded_bins), _ptr(positions), T,
+              H, padded_bins.numel(), top_k, _ptr(out), out_rows, _ptr(status), _stream(x))
     return out
 
 
 def moe_binned_gather_weighted(dy: torch.Tensor, indices: torch.Tensor, bins: torch.Tensor, weights: torch.Tensor,
                                num_experts: int, capacity: int, top_k: int, out: torch.Tensor | None = None,
-                               status: torch.Tensor | None = None) -> torch.Tensor:
+                               status: torch.Tensor | None = None,
+                               positions: torch.Tensor | None = None) -> torch.Tensor:
     """Gradient of the binned combine with respect to the expert rows:
     dy [T, H] -> [E, capacity, H], row of kept a = weights[a] * dy[a // K]."""
     _need(dy, None, "dy")
@@ -148,18 +163,22 @@ def moe_binned_gather_weighted(dy: torch.Tensor, indices: torch.Tensor, bins: to
     _need(indices, torch.int32, "indices", dy.device)
     _need(bins, torch.int32, "bins", dy.device)
     _need(weights, torch.float32, "weights", dy.device)
+    if positions is not None:
+        _need(positions, torch.int32, "positions", dy.device)
+        _need_numel(positions, T * top_k, "positions")
     if out is None:
         out = torch.empty((num_experts, capacity, H), dtype=dy.dtype, device=dy.device)
     _need(out, dy.dtype, "out", dy.device)
-    _lib.call("moe_binned_gather_weighted", _ptr(dy), dt, _ptr(indices), _ptr(bins), _ptr(weights), T, H,
-              num_experts, capacity, top_k, _ptr(out), _ptr(status), _stream(dy))
+    _lib.call("moe_binned_gather_weighted", _ptr(dy), dt, _ptr(indices), _ptr(bins), _ptr(weights),
+              _ptr(positions), T, H, num_experts, capacity, top_k, _ptr(out), _ptr(status), _stream(dy))
     return out
 
 
 def moe_padded_gather_weighted(dy: torch.Tensor, indices: torch.Tensor, bins: torch.Tensor,
                                padded_bins: torch.Tensor, weights: torch.Tensor, top_k: int,
                                out_rows: int | None = None, out: torch.Tensor | None = None,
-                               status: torch.Tensor | None = None) -> torch.Tensor:
+                               status: torch.Tensor | None = None,
+                               positions: torch.Tensor | None = None) -> torch.Tensor:
     """Gradient of the padded combine with respect to the expert rows."""
     _need(dy, None, "dy")
     dt = _act_dtype(dy, "dy")
@@ -168,13 +187,17 @@ def moe_padded_gather_weighted(dy: torch.Tensor, indices: torch.Tensor, bins: to
     _need(bins, torch.int32, "bins", dy.device)
     _need(padded_bins, torch.int32, "padded_bins", dy.device)
     _need(weights, torch.float32, "weights", dy.device)
+    if positions is not None:
+        _need(positions, torch.int32, "positions", dy.device)
+        _need_numel(positions, T * top_k, "positions")
     if out_rows is None:
         out_rows = int(padded_bins[-1].item()) if out is None else out.shape[0]
     if out is None:
         out = torch.empty((out_rows, H), dtype=dy.dtype, device=dy.device)
     _need(out, dy.dtype, "out", dy.device)
     _lib.call("moe_padded_gather_weighted", _ptr(dy), dt, _ptr(indices), _ptr(bins), _ptr(padded_bins),
-              _ptr(weights), T, H, padded_bins.numel(), top_k, _ptr(out), out_rows, _ptr(status), _stream(dy))
+              _ptr(weights), _ptr(positions), T, H, padded_bins.numel(), top_k, _ptr(out), out_rows, _ptr(status),
+              _stream(dy))
     return out
 
 
@@ -259,6 +282,7 @@ def moe_binned_scatter(xe: torch.Tensor, indices: torch.Tensor, bin_ids: torch.T
         _need(weights, torch.float32, "weights", xe.device)
     if positions is not None:
         _need(positions, torch.int32, "positions", xe.device)
+        _need_numel(positions, num_tokens * top_k, "positions")
     if out is None:
         out = torch.empty((num_tokens, H), dtype=xe.dtype, device=xe.device)
     _need(out, xe.dtype, "out", xe.device)
@@ -285,6 +309,7 @@ def moe_padded_scatter(xe: torch.Tensor, indices: torch.Tensor, bin_ids: torch.T
         _need(weights, torch.float32, "weights", xe.device)
     if positions is not None:
         _need(positions, torch.int32, "positions", xe.device)
+        _need_numel(positions, num_tokens * top_k, "positions")
     if out is None:
         out = torch.empty((num_tokens, H), dtype=xe.dtype, device=xe.device)
     _need(out, xe.dtype, "out", xe.device)
@@ -318,8 +343,9 @@ def moe_binned_wgrad(xe: torch.Tensor, grad: torch.Tensor, indices: torch.Tensor
 
 def moe_padded_wgrad(xe: torch.Tensor, grad: torch.Tensor, indices: torch.Tensor, bin_ids: torch.Tensor,
                      bins: torch.Tensor, padded_bins: torch.Tensor, top_k: int, out: torch.Tensor | None = None,
-                     status: torch.Tensor | None = None) -> torch.Tensor:
-    """Router-weight gradient [T*K] fp32 of the padded combine."""
+                     status: torch.Tensor | None = None, positions: torch.Tensor | None = None) -> torch.Tensor:
+    """Router-weight gradient [T*K] fp32 of the padded combine. ``positions``
+    as for moe_binned_gather (one launch instead of two)."""
     _need(xe, None, "xe")
     dt = _act_dtype(xe, "xe")
     rows, H = xe.shape
@@ -327,11 +353,15 @@ def moe_padded_wgrad(xe: torch.Tensor, grad: torch.Tensor, indices: torch.Tensor
     T = grad.shape[0]
     for t, nm in ((indices, "indices"), (bin_ids, "bin_ids"), (bins, "bins"), (padded_bins, "padded_bins")):
         _need(t, torch.int32, nm, xe.device)
+    if positions is not None:
+        _need(positions, torch.int32, "positions", xe.device)
+        _need_numel(positions, T * top_k, "positions")
     if out is None:
         out = torch.empty(T * top_k, dtype=torch.float32, device=xe.device)
     _need(out, torch.float32, "out", xe.device)
     _lib.call("moe_padded_wgrad", _ptr(xe), _ptr(grad), dt, _ptr(indices), _ptr(bin_ids), _ptr(bins),
-              _ptr(padded_bins), T, H, padded_bins.numel(), top_k, rows, _ptr(out), _ptr(status), _stream(xe))
+              _ptr(padded_bins), _ptr(positions), T, H, padded_bins.numel(), top_k, rows, _ptr(out), _ptr(status),
+              _stream(xe))
     return out
 
 

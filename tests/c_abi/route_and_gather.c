@@ -71,7 +71,8 @@ int main(int argc, char** argv) {
   CHECK_CUDA(cudaStreamCreate(&s));
 
   CHECK_MOE(moe_route_build(d_te, n, E, m, d_idx, d_bid, d_bins, d_pb, d_pos, d_ws, ws, d_status, s));
-  CHECK_MOE(moe_binned_gather(d_x, MOE_F32, d_idx, d_bins, T, H, E, cap, K, d_xb, d_status, s));
+  /* binned gather without positions (it builds its own), padded gather with the route build's */
+  CHECK_MOE(moe_binned_gather(d_x, MOE_F32, d_idx, d_bins, NULL, T, H, E, cap, K, d_xb, d_status, s));
   CHECK_MOE(moe_binned_scatter(d_xb, MOE_F32, d_idx, d_bid, d_bins, NULL, d_pos, T, H, E, cap, K, d_y, NULL, 0,
                                d_status, s));
   int32_t* bins = malloc(E * 4);
@@ -80,7 +81,7 @@ int main(int argc, char** argv) {
   CHECK_CUDA(cudaStreamSynchronize(s));
   const int64_t P = pb[E - 1];  /* the caller reads the padded row count back to size the output */
   CHECK_CUDA(cudaMalloc((void**)&d_xp, (P > 0 ? P : 1) * H * 4));
-  CHECK_MOE(moe_padded_gather(d_x, MOE_F32, d_idx, d_bins, d_pb, T, H, E, K, d_xp, P, d_status, s));
+  CHECK_MOE(moe_padded_gather(d_x, MOE_F32, d_idx, d_bins, d_pb, d_pos, T, H, E, K, d_xp, P, d_status, s));
   CHECK_CUDA(cudaStreamSynchronize(s));
 
   int32_t *idx = malloc(n * 4), *bid = malloc(n * 4), *pos = malloc(n * 4), status = 0;

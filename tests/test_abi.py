@@ -59,26 +59,31 @@ def test_host_validation_rejects_bad_arguments(lib):
     # padded total overflowing int32
     assert lib.moe_route_build(FAKE, 2**31 - 10, 4, 8, FAKE, FAKE, FAKE, FAKE, None, FAKE, 1 << 40, None, None) == 1
     # gather: bad dtype, negative capacity, top_k out of range, T*K overflow, misaligned x
-    assert lib.moe_binned_gather(FAKE, 7, FAKE, FAKE, 4, 8, 2, 2, 1, FAKE, None, None) == 2
-    assert lib.moe_binned_gather(FAKE, 0, FAKE, FAKE, 4, 8, 2, -1, 1, FAKE, None, None) == 1
-    assert lib.moe_binned_gather(FAKE, 0, FAKE, FAKE, 4, 8, 2, 2, 0, FAKE, None, None) == 1
-    assert lib.moe_binned_gather(FAKE, 0, FAKE, FAKE, 4, 8, 2, 2, 65, FAKE, None, None) == 1
-    assert lib.moe_binned_gather(FAKE, 0, FAKE, FAKE, 2**30, 8, 2, 2, 4, FAKE, None, None) == 1
-    assert lib.moe_binned_gather(FAKE + 2, 0, FAKE, FAKE, 4, 8, 2, 2, 1, FAKE, None, None) == 2
-    assert lib.moe_padded_gather(FAKE, 1, FAKE, FAKE, None, 4, 8, 2, 1, FAKE, 8, None, None) == 1
-    assert lib.moe_padded_gather(FAKE, 1, FAKE, FAKE, FAKE, 4, 8, 2, 1, FAKE, -1, None, None) == 1
+    assert lib.moe_binned_gather(FAKE, 7, FAKE, FAKE, None, 4, 8, 2, 2, 1, FAKE, None, None) == 2
+    assert lib.moe_binned_gather(FAKE, 0, FAKE, FAKE, None, 4, 8, 2, -1, 1, FAKE, None, None) == 1
+    assert lib.moe_binned_gather(FAKE, 0, FAKE, FAKE, None, 4, 8, 2, 2, 0, FAKE, None, None) == 1
+    assert lib.moe_binned_gather(FAKE, 0, FAKE, FAKE, None, 4, 8, 2, 2, 65, FAKE, None, None) == 1
+    assert lib.moe_binned_gather(FAKE, 0, FAKE, FAKE, None, 2**30, 8, 2, 2, 4, FAKE, None, None) == 1
+    assert lib.moe_binned_gather(FAKE + 2, 0, FAKE, FAKE, None, 4, 8, 2, 2, 1, FAKE, None, None) == 2
+    assert lib.moe_padded_gather(FAKE, 1, FAKE, FAKE, None, None, 4, 8, 2, 1, FAKE, 8, None, None) == 1
+    assert lib.moe_padded_gather(FAKE, 1, FAKE, FAKE, FAKE, None, 4, 8, 2, 1, FAKE, -1, None, None) == 1
+    # misaligned positions
+    assert lib.moe_binned_gather(FAKE, 0, FAKE, FAKE, FAKE + 2, 4, 8, 2, 2, 1, FAKE, None, None) == 2
+    assert lib.moe_padded_gather(FAKE, 0, FAKE, FAKE, FAKE, FAKE + 2, 4, 8, 2, 1, FAKE, 8, None, None) == 2
+    assert lib.moe_padded_wgrad(FAKE, FAKE, 0, FAKE, FAKE, FAKE, FAKE, FAKE + 2, 4, 8, 2, 1, 8, FAKE, None,
+                                None) == 2
     # scatter without positions needs a workspace
     assert lib.moe_binned_scatter(FAKE, 0, FAKE, FAKE, FAKE, None, None, 4, 8, 2, 4, 1, FAKE, None, 0, None,
                                   None) == 1
     assert lib.moe_padded_scatter(FAKE, 1, FAKE, FAKE, FAKE, None, None, None, 4, 8, 2, 1, 8, FAKE, None, 0, None,
                                   None) == 1
     assert lib.moe_binned_wgrad(FAKE, None, 0, FAKE, FAKE, FAKE, 4, 8, 2, 4, 1, FAKE, None, None) == 1
-    assert lib.moe_padded_wgrad(FAKE, FAKE, 0, FAKE, FAKE, FAKE, FAKE, 4, 8, 2, 1, -3, FAKE, None, None) == 1
+    assert lib.moe_padded_wgrad(FAKE, FAKE, 0, FAKE, FAKE, FAKE, FAKE, None, 4, 8, 2, 1, -3, FAKE, None, None) == 1
     # weighted gather: weights required when there are tokens; misaligned weights
-    assert lib.moe_binned_gather_weighted(FAKE, 1, FAKE, FAKE, None, 4, 8, 2, 2, 1, FAKE, None, None) == 1
-    assert lib.moe_binned_gather_weighted(FAKE, 1, FAKE, FAKE, FAKE + 2, 4, 8, 2, 2, 1, FAKE, None, None) == 2
-    assert lib.moe_padded_gather_weighted(FAKE, 0, FAKE, FAKE, None, FAKE, 4, 8, 2, 1, FAKE, 8, None, None) == 1
-    assert lib.moe_padded_gather_weighted(FAKE, 0, FAKE, FAKE, FAKE, None, 4, 8, 2, 1, FAKE, 8, None, None) == 1
+    assert lib.moe_binned_gather_weighted(FAKE, 1, FAKE, FAKE, None, None, 4, 8, 2, 2, 1, FAKE, None, None) == 1
+    assert lib.moe_binned_gather_weighted(FAKE, 1, FAKE, FAKE, FAKE + 2, None, 4, 8, 2, 2, 1, FAKE, None, None) == 2
+    assert lib.moe_padded_gather_weighted(FAKE, 0, FAKE, FAKE, None, FAKE, None, 4, 8, 2, 1, FAKE, 8, None, None) == 1
+    assert lib.moe_padded_gather_weighted(FAKE, 0, FAKE, FAKE, FAKE, None, None, 4, 8, 2, 1, FAKE, 8, None, None) == 1
     # route build + gather in one call: positions required, padded_bins required for the padded layout,
     # bad dtype, workspace too small, negative out_rows (all before anything is enqueued)
     ws2 = lib.moe_route_build_workspace_size(8, 2)
@@ -113,8 +118,8 @@ def test_host_validation_rejects_bad_arguments(lib):
 
 def test_empty_problems_enqueue_nothing(lib):
     # Zero rows / zero tokens return MOE_OK without launching anything.
-    assert lib.moe_binned_gather(FAKE, 0, FAKE, FAKE, 4, 8, 2, 0, 1, FAKE, None, None) == 0
-    assert lib.moe_padded_gather(FAKE, 0, FAKE, FAKE, FAKE, 4, 8, 2, 1, FAKE, 0, None, None) == 0
+    assert lib.moe_binned_gather(FAKE, 0, FAKE, FAKE, None, 4, 8, 2, 0, 1, FAKE, None, None) == 0
+    assert lib.moe_padded_gather(FAKE, 0, FAKE, FAKE, FAKE, None, 4, 8, 2, 1, FAKE, 0, None, None) == 0
     assert lib.moe_binned_scatter(FAKE, 0, FAKE, FAKE, FAKE, None, FAKE, 0, 8, 2, 4, 1, FAKE, None, 0, None,
                                   None) == 0
     assert lib.moe_binned_wgrad(FAKE, FAKE, 0, FAKE, FAKE, FAKE, 0, 8, 2, 4, 1, FAKE, None, None) == 0

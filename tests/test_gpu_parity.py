@@ -66,12 +66,15 @@ def run_routing(r: wl.Routing, binned=True, padded=True, poison=True, misalign=F
         x, grad = misaligned_like(x), misaligned_like(grad)
     w = to_dev(r.weights.reshape(-1), DEV)
     pos = route.positions if pass_positions else None
+    # gathers and the padded wgrad run with the route's positions and without (they build their own)
+    pos_variants = (pos, None) if pos is not None else (None,)
 
     if binned:
         cap = r.capacity
-        xb = p.moe_binned_gather(x, route.indices, route.bins, E, cap, K, status=st)
         o_xb = oracle.binned_gather(r.x, o["indices"], o["bin_ids"], o["bins"], E, cap, K)
-        assert_bits_equal(to_host(xb), o_xb, r.name + " binned_gather")
+        for gp in pos_variants:
+            xb = p.moe_binned_gather(x, route.indices, route.bins, E, cap, K, status=st, positions=gp)
+            assert_bits_equal(to_host(xb), o_xb, "%s binned_gather (positions %s)" % (r.name, gp is not None))
         xe_np = wl.expert_rows(E * cap, H, r.dtype, r.seed).reshape(E, cap, H)
         if poison and cap > 0:
             # unused capacity rows hold NaN: scatter and wgrad must never read them
@@ -93,15 +96,18 @@ def run_routing(r: wl.Routing, binned=True, padded=True, poison=True, misalign=F
         wg = p.moe_binned_wgrad(xe, grad, route.indices, route.bin_ids, route.bins, K, status=st)
         o_wg = oracle.binned_wgrad(xe_np, r.grad, o["indices"], o["bin_ids"], o["bins"], K)
         assert_close_fp32(to_host(wg), o_wg, r.name + " binned_wgrad")
-        gw = p.moe_binned_gather_weighted(grad, route.indices, route.bins, w, E, cap, K, status=st)
         o_gw = oracle.binned_gather_weighted(r.grad, o["indices"], o["bin_ids"], o["bins"], r.weights, E, cap, K)
-        assert_bits_equal(to_host(gw), o_gw, r.name + " binned_gather_weighted")
+        for gp in pos_variants:
+            gw = p.moe_binned_gather_weighted(grad, route.indices, route.bins, w, E, cap, K, status=st, positions=gp)
+            assert_bits_equal(to_host(gw), o_gw, "%s binned_gather_weighted (positions %s)" % (r.name, gp is not None))
 
     if padded:
         P = int(o["padded_bins"][-1]) if E else 0
-        xp = p.moe_padded_gather(x, route.indices, route.bins, route.padded_bins, K, out_rows=P, status=st)
         o_xp = oracle.padded_gather(r.x, o["indices"], o["bin_ids"], o["bins"], o["padded_bins"], K)
-        assert_bits_equal(to_host(xp), o_xp, r.name + " padded_gather")
+        for gp in pos_variants:
+            xp = p.moe_padded_gather(x, route.indices, route.bins, route.padded_bins, K, out_rows=P, status=st,
+                                     positions=gp)
+            assert_bits_equal(to_host(xp), o_xp, "%s padded_gather (positions %s)" % (r.name, gp is not None))
         xe_np = wl.expert_rows(P, H, r.dtype, r.seed)
         if poison:
             real = np.zeros(P, bool)
@@ -118,14 +124,17 @@ def run_routing(r: wl.Routing, binned=True, padded=True, poison=True, misalign=F
                                      positions=pos, status=st)
             o_y = oracle.padded_scatter(xe_np, o["indices"], o["bin_ids"], o["bins"], o["padded_bins"], o_w, T, K)
             check_scatter(to_host(y), o_y, "%s padded_scatter %s" % (r.name, tag))
-        wg = p.moe_padded_wgrad(xe, grad, route.indices, route.bin_ids, route.bins, route.padded_bins, K, status=st)
         o_wg = oracle.padded_wgrad(xe_np, r.grad, o["indices"], o["bin_ids"], o["bins"], o["padded_bins"], K)
-        assert_close_fp32(to_host(wg), o_wg, r.name + " padded_wgrad")
-        gw = p.moe_padded_gather_weighted(grad, route.indices, route.bins, route.padded_bins, w, K, out_rows=P,
-                                          status=st)
         o_gw = oracle.padded_gather_weighted(r.grad, o["indices"], o["bin_ids"], o["bins"], o["padded_bins"],
                                              r.weights, K)
-        assert_bits_equal(to_host(gw), o_gw, r.name + " padded_gather_weighted")
+        for gp in pos_variants:
+            tag = "(positions %s)" % (gp is not None)
+            wg = p.moe_padded_wgrad(xe, grad, route.indices, route.bin_ids, route.bins, route.padded_bins, K,
+                                    status=st, positions=gp)
+            assert_close_fp32(to_host(wg), o_wg, "%s padded_wgrad %s" % (r.name, tag))
+            gw = p.moe_padded_gather_weighted(grad, route.indices, route.bins, route.padded_bins, w, K, out_rows=P,
+                                              status=st, positions=gp)
+            assert_bits_equal(to_host(gw), o_gw, "%s padded_gather_weighted %s" % (r.name, tag))
     torch.cuda.synchronize()
     assert int(st.item()) == 0, "device status %d on valid input" % int(st.item())
 
@@ -426,6 +435,19 @@ def test_corrupt_bins_and_positions_are_reported():
     y = p.moe_binned_scatter(xe, route.indices, route.bin_ids, route.bins, None, 32, 2, positions=bad_pos, status=st)
     torch.cuda.synchronize()
     assert int(st.item()) & _lib.MOE_STATUS_BAD_INDEX
+    # the same positions handed to the gathers and the padded wgrad: checked, flagged, never followed
+    for what, run in (
+            ("binned gather", lambda s_: p.moe_binned_gather(x, route.indices, route.bins, 4, 8, 2, status=s_,
+                                                             positions=bad_pos)),
+            ("padded gather", lambda s_: p.moe_padded_gather(x, route.indices, route.bins, route.padded_bins, 2,
+                                                             out_rows=80, status=s_, positions=bad_pos)),
+            ("padded wgrad", lambda s_: p.moe_padded_wgrad(torch.randn(80, 16, device=DEV), x, route.indices,
+                                                           route.bin_ids, route.bins, route.padded_bins, 2,
+                                                           status=s_, positions=bad_pos))):
+        st.zero_()
+        run(st)
+        torch.cuda.synchronize()
+        assert int(st.item()) & _lib.MOE_STATUS_BAD_INDEX, what
     assert not to_host(y).any()  # every slot skipped
     st.zero_()
     pb = torch.tensor([4, 8, 12, 20], dtype=torch.int32, device=DEV)

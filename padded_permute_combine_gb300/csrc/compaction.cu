@@ -10,9 +10,12 @@
 // -1 / 0.0f.
 // Rows of at most 64 experts with topk <= 8 take one thread per row instead
 // (32 rows per warp in flight).
-// Backward: one thread per 16 dense columns when rows are whole 16-column
-// chunks and topk <= 8 (the row's slots loaded once, four float4 stores of
-// zeros, the slots stored over them);
+// Backward: for rows of at most 2048 experts in whole float4s, a warp builds
+// a block of consecutive rows in shared memory and stores it with coalesced
+// 16-byte stores; else one thread per 16
+// dense columns when rows are whole 16-column chunks and topk <= 8 (the
+// row's slots loaded once, four float4 stores of zeros, the slots stored
+// over them);
 // else one warp per row when the row is whole float4s (slots broadcast by
 // shuffles, one float4 store per lane and 128-column chunk); other shapes
 // take one thread per dense output, scanning the row's slots.
@@ -22,6 +25,8 @@ namespace moe {
 namespace {
 
 constexpr int kThreads = 256;
+
+
 
 // Bit b of the result is set when byte b of w is nonzero.
 __device__ __forceinline__ unsigned nonzero_bytes(uint32_t w) {
@@ -190,6 +195,70 @@ __global__ void __launch_bounds__(kThreads)
       const unsigned d = (unsigned)(e[j] - c0);
       if (d < 16u) row[d] = v[j];
     }
+  }
+}
+
+// Staged backward for rows of at most kStageFloats = 2048 experts in
+// whole float4s: a warp takes R = min(32, 2048 / E) consecutive rows at a
+// time (32 rows of the Qwen2-MoE-57B shape, E = 64; 8 of the DeepSeek-V3
+// shape, E = 256). Their dense fp32 rows are one contiguous block of at
+// most 8 KB, built in the warp's slice of shared memory (zeroed, then lane
+// r < R stores row r's slots in increasing slot order, so a repeated index
+// keeps the highest slot) and written to HBM with coalesced 16-byte stores
+// (lane l takes chunks l, l+32, ...): every dense element is written once,
+// as part of whole lines. (A staged forward, which loads the whole
+// probability block in the same round as the map, measured slower than
+// reading the routed entries directly: 10.2 vs 8.4 us at 65 536 x 64.)
+constexpr int kStageWarps = 4;
+constexpr int kStageThreads = kStageWarps * kWarp;
+constexpr int kStageFloats = 2048;           // one warp's block: 8 KB
+constexpr int kStageChunks = kStageFloats / 4;
+
+__global__ void __launch_bounds__(kStageThreads)
+    compaction_bwd_staged_kernel(const float* __restrict__ gpi, const int32_t* __restrict__ indices, int64_t T,
+                                 int32_t E, int32_t topk, float* __restrict__ grad_probs, int32_t* status) {
+  await_previous_kernel();
+  __shared__ float4 stage[kStageWarps][kStageChunks];
+  const int warp = threadIdx.x / kWarp, lane = lane_id();
+  const int R = min(kWarp, kStageFloats / E);  // rows per block
+  float4* blk = stage[warp];
+  float* srow = reinterpret_cast<float*>(blk) + lane * E;
+  for (int64_t t0 = ((int64_t)blockIdx.x * kStageWarps + warp) * R; t0 < T;
+       t0 += (int64_t)gridDim.x * kStageWarps * R) {
+    const int rows = (int)min((int64_t)R, T - t0);
+    const int nchunk = rows * E / 4;
+    int32_t e[8];
+    float v[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      e[j] = -1;
+      v[j] = 0.0f;
+      if (j < topk && lane < rows) {
+        e[j] = __ldg(indices + (t0 + lane) * topk + j);
+        v[j] = __ldg(gpi + (t0 + lane) * topk + j);
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < kStageChunks / kWarp; ++u) {
+      const int c = u * kWarp + lane;
+      if (c < nchunk) blk[c] = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+    }
+    __syncwarp();
+    bool bad = false;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      if ((unsigned)e[j] < (unsigned)E) srow[e[j]] = v[j];
+      else bad |= e[j] != -1;
+    }
+    if (__any_sync(0xffffffffu, bad) && lane == 0) flag_status(status, MOE_STATUS_BAD_INDEX);
+    __syncwarp();
+    float4* dst = reinterpret_cast<float4*>(grad_probs + t0 * E);
+#pragma unroll
+    for (int u = 0; u < kStageChunks / kWarp; ++u) {
+      const int c = u * kWarp + lane;
+      if (c < nchunk) dst[c] = blk[c];
+    }
+    __syncwarp();  // the block is read before it is zeroed again
   }
 }
 
@@ -364,7 +433,13 @@ extern "C" int moe_routing_map_to_indices_bwd(const float* grad_probs_indices, c
     return MOE_ERR_UNSUPPORTED;
   if (T == 0) return MOE_OK;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  if (E % 16 == 0 && topk <= 8 && aligned(grad_probs, 16)) {
+  if (E <= kStageFloats && E % 4 == 0 && topk <= 8 && aligned(grad_probs, 16)) {
+    auto k = compaction_bwd_staged_kernel;
+    const int64_t rows = kStageFloats / E < kWarp ? kStageFloats / E : kWarp;
+    const int64_t ctas = (T + rows * kStageWarps - 1) / (rows * kStageWarps);
+    launch(k, persistent_grid(k, kStageThreads, 0, ctas), kStageThreads, 0, s, grad_probs_indices, indices, T, E,
+           topk, grad_probs, d_status);
+  } else if (E % 16 == 0 && topk <= 8 && aligned(grad_probs, 16)) {
     auto k = compaction_bwd_chunk_kernel;
     launch(k, grid_for(k, T * (E / 16)), kThreads, 0, s, grad_probs_indices, indices, T, E, topk, grad_probs, d_status);
   } else if (E % 4 == 0 && aligned(grad_probs, 16)) {

@@ -248,10 +248,10 @@ int moe_padded_gather_weighted(const void* dy, int32_t dtype,
  * Route build and gather in one call ([padded] Workflow steps 1-5;
  * [binned] Workflow steps 1-3): exactly moe_route_build of
  * top_expert [n = T*top_k] (all five outputs, positions required) followed
- * by moe_binned_gather / moe_padded_gather of x, with the same results. The
- * gather reads the positions the route build has just written, so it needs
- * neither its inverse-permutation pass nor the borrowed output tail: four
- * launches instead of six, and x is read once per token.
+ * by moe_binned_gather / moe_padded_gather of x given those positions, with
+ * the same results: four launches (the route build's three and the
+ * gather's token pass), x read once per token. Its value over the two calls
+ * is that the caller needs no positions buffer of its own between them.
  *   workspace: >= moe_route_build_workspace_size(n, E) bytes.
  *   padded: out has out_rows rows; the caller does not know
  *   padded_bins[E-1] before the call, so out_rows is a bound, such as

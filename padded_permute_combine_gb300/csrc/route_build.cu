@@ -2,7 +2,8 @@
 // ("Build Triton-Ascend Padded MoE Routing", Workflow steps 1-3;
 //  "Build Triton-Ascend Binned MoE Routing", Workflow steps 1-2).
 //
-// Three launches, no inter-CTA waiting:
+// Three launches, no inter-CTA waiting (two when chunks x experts is small:
+// the scatter CTAs then each do the scan's work for themselves):
 //   1. hist:    CTA g counts the expert ids of its chunk -> counts[g][e].
 //   2. scan:    one CTA turns each expert's column of counts into a prefix
 //               over chunks and writes bins and padded_bins.
@@ -24,6 +25,13 @@ constexpr int kRounds = 4;      // 32-element rounds per warp and chunk
 constexpr int kMaxWarps = 16;   // warps per CTA of the hist / scatter passes
 constexpr int kSmemBudget = 48 * 1024;  // per-warp counters of the scatter pass
 constexpr int kScanThreads = 1024;
+// The scan folds into the scatter pass (two launches instead of three) when
+// every scatter CTA can afford to read the whole chunk x expert count matrix.
+#ifndef MOE_ROUTE_FUSED_MAX_COUNTS
+#define MOE_ROUTE_FUSED_MAX_COUNTS 16384
+#endif
+constexpr int64_t kFusedMaxCounts = MOE_ROUTE_FUSED_MAX_COUNTS;
+constexpr int32_t kFusedMaxExperts = 256;
 
 struct RouteShape {
   int warps;      // warps per CTA of the hist / scatter passes
@@ -142,14 +150,97 @@ __global__ void __launch_bounds__(kScanThreads) route_scan_kernel(int32_t* __res
   }
 }
 
+// Exclusive block scan over experts of v[e] (in place) and of its rounding
+// up to multiples of m (into pv, when pv is not null); every thread of the
+// block takes part. Returns nothing; the inclusive values are v + count.
+__device__ void block_scan_experts(int64_t* v, int64_t* pv, int32_t E, int32_t m, int64_t (*warp_sum)[2]) {
+  const int nt = blockDim.x, lane = lane_id(), warp = threadIdx.x / kWarp;
+  const int per = (E + nt - 1) / nt;
+  const int lo = threadIdx.x * per;
+  const int hi = min(lo + per, (int)E);
+  int64_t s = 0, ps = 0;
+  for (int e = lo; e < hi; ++e) {
+    s += v[e];
+    ps += (v[e] + m - 1) / m * m;
+  }
+  int64_t xs = s, xps = ps;
+#pragma unroll
+  for (int d = 1; d < kWarp; d <<= 1) {
+    const int64_t a = __shfl_up_sync(0xffffffffu, xs, d);
+    const int64_t b = __shfl_up_sync(0xffffffffu, xps, d);
+    if (lane >= d) { xs += a; xps += b; }
+  }
+  if (lane == kWarp - 1) { warp_sum[warp][0] = xs; warp_sum[warp][1] = xps; }
+  __syncthreads();
+  if (warp == 0) {
+    const int nw = nt / kWarp;
+    int64_t a = lane < nw ? warp_sum[lane][0] : 0, b = lane < nw ? warp_sum[lane][1] : 0;
+#pragma unroll
+    for (int d = 1; d < kWarp; d <<= 1) {
+      const int64_t ua = __shfl_up_sync(0xffffffffu, a, d);
+      const int64_t ub = __shfl_up_sync(0xffffffffu, b, d);
+      if (lane >= d) { a += ua; b += ub; }
+    }
+    if (lane < nw) { warp_sum[lane][0] = a; warp_sum[lane][1] = b; }
+  }
+  __syncthreads();
+  int64_t run = xs - s + (warp > 0 ? warp_sum[warp - 1][0] : 0);
+  int64_t prun = xps - ps + (warp > 0 ? warp_sum[warp - 1][1] : 0);
+  for (int e = lo; e < hi; ++e) {
+    const int64_t c = v[e];
+    v[e] = run;
+    run += c;
+    if (pv != nullptr) {
+      pv[e] = prun;
+      prun += (c + m - 1) / m * m;
+    }
+  }
+  __syncthreads();
+}
+
+// FUSED (few chunks, E <= kFusedMaxExperts): `offsets` holds the raw
+// per-chunk counts of the hist pass and every CTA derives what the scan pass
+// would have given it — its column prefix over the chunks before it and the
+// exclusive scan over experts of the totals — from the whole count matrix
+// (read from L2); CTA 0 also writes bins and padded_bins. One launch fewer,
+// and still no CTA waits on another.
+template <bool FUSED>
 __global__ void route_scatter_kernel(const int32_t* __restrict__ top_expert, int64_t n, int32_t E,
-                                     const int32_t* __restrict__ offsets, const int32_t* __restrict__ bins, int32_t* __restrict__ indices,
-                                     int32_t* __restrict__ bin_ids, int32_t* __restrict__ positions) {
+                                     const int32_t* __restrict__ offsets, int64_t G, int32_t m,
+                                     int32_t* __restrict__ bins, int32_t* __restrict__ padded_bins,
+                                     int32_t* __restrict__ indices, int32_t* __restrict__ bin_ids,
+                                     int32_t* __restrict__ positions) {
   await_previous_kernel();
-  extern __shared__ int32_t whist[];  // [warps][E]: per-warp running offsets
+  extern __shared__ int32_t whist[];  // [warps][E]: per-warp running offsets; FUSED: then 4 x [E] int64
+  __shared__ int64_t warp_sum[kMaxWarps][2];
   const int warps = blockDim.x / kWarp;
   const int warp = threadIdx.x / kWarp, lane = lane_id();
   for (int q = threadIdx.x; q < warps * E; q += blockDim.x) whist[q] = 0;
+  int64_t* spre = reinterpret_cast<int64_t*>(whist + ((warps * E + 1) & ~1));  // prefix over earlier chunks
+  int64_t* stot = spre + E;                                                     // total per expert
+  int64_t* sst = stot + E;                                                      // exclusive start per expert
+  int64_t* spst = sst + E;                                                      // padded start (CTA 0)
+  if (FUSED) {
+    for (int e = threadIdx.x; e < E; e += blockDim.x) {
+      int64_t pre = 0, tot = 0;
+      for (int64_t g = 0; g < G; ++g) {
+        const int32_t c = __ldg(offsets + g * E + e);
+        pre += g < (int64_t)blockIdx.x ? c : 0;
+        tot += c;
+      }
+      spre[e] = pre;
+      stot[e] = tot;
+      sst[e] = tot;
+    }
+    __syncthreads();
+    block_scan_experts(sst, blockIdx.x == 0 ? spst : nullptr, E, m, warp_sum);
+    if (blockIdx.x == 0) {
+      for (int e = threadIdx.x; e < E; e += blockDim.x) {
+        bins[e] = (int32_t)(sst[e] + stot[e]);
+        if (padded_bins != nullptr) padded_bins[e] = (int32_t)(spst[e] + (stot[e] + m - 1) / m * m);
+      }
+    }
+  }
   __syncthreads();
   const int64_t base = (int64_t)blockIdx.x * blockDim.x * kRounds + (int64_t)warp * kWarp * kRounds;
   int32_t* mine = whist + warp * E;
@@ -163,7 +254,7 @@ __global__ void route_scatter_kernel(const int32_t* __restrict__ top_expert, int
   }
   __syncthreads();
   for (int e = threadIdx.x; e < E; e += blockDim.x) {
-    int32_t run = offsets[(int64_t)blockIdx.x * E + e] + (e > 0 ? bins[e - 1] : 0);
+    int32_t run = FUSED ? (int32_t)(spre[e] + sst[e]) : offsets[(int64_t)blockIdx.x * E + e] + (e > 0 ? bins[e - 1] : 0);
     for (int w = 0; w < warps; ++w) {
       const int32_t c = whist[w * E + e];
       whist[w * E + e] = run;
@@ -219,9 +310,16 @@ extern "C" int moe_route_build(const int32_t* top_expert, int64_t n, int32_t E, 
   int32_t* counts = static_cast<int32_t*>(workspace);
   const int threads = shape.warps * kWarp;
   launch(route_hist_kernel, (unsigned)shape.ctas, threads, E * sizeof(int32_t), s, top_expert, n, E, counts, d_status);
+  const size_t whist_bytes = (size_t)shape.warps * E * sizeof(int32_t);
+  if (n > 0 && E <= kFusedMaxExperts && shape.ctas * E <= kFusedMaxCounts) {
+    const size_t smem = (whist_bytes + 7) / 8 * 8 + 4 * (size_t)E * sizeof(int64_t);
+    launch(route_scatter_kernel<true>, (unsigned)shape.ctas, threads, smem, s, top_expert, n, E, counts, shape.ctas,
+           pad_multiple, bins, padded_bins, indices, bin_ids, positions);
+    return check_launch();
+  }
   launch(route_scan_kernel, 1, kScanThreads, 0, s, counts, shape.ctas, E, pad_multiple, bins, padded_bins);
   if (n > 0)
-    launch(route_scatter_kernel, (unsigned)shape.ctas, threads, (size_t)shape.warps * E * sizeof(int32_t), s,
-           top_expert, n, E, counts, bins, indices, bin_ids, positions);
+    launch(route_scatter_kernel<false>, (unsigned)shape.ctas, threads, whist_bytes, s, top_expert, n, E, counts,
+           shape.ctas, pad_multiple, bins, padded_bins, indices, bin_ids, positions);
   return check_launch();
 }

@@ -111,6 +111,15 @@ def traffic_from_profiles(kernel: str, digest: str):
     return None
 
 
+def route_build_launches(n: int, E: int) -> int:
+    """Kernels one moe_route_build launches: hist, scan, scatter; the scan
+    folds into the scatter pass when chunks x experts <= 16384 and E <= 256
+    (chunks of 2048 assignments for E <= 768)."""
+    warps = max(1, min(16, (48 * 1024) // (4 * E)))
+    chunks = max(1, -(-n // (warps * 32 * 4)))
+    return 2 if (n > 0 and E <= 256 and chunks * E <= 16384) else 3
+
+
 def l2_flush(buf) -> None:
     """Evicts L2 before a timed launch: writes `buf` (512 MB of fp32, four
     times L2), then reads it back in place (an fp32 sum makes no widened
@@ -214,7 +223,8 @@ class Path:
         return [
             ("compaction_fwd", 1, lambda: p.moe_routing_map_to_indices_fwd(self.probs, self.rmap, K,
                                                                            out=(self.pi, self.idx))),
-            ("route_build", 3, lambda: p.moe_route_build(self.idx, E, r.pad_multiple, workspace=self.ws, out=rt)),
+            ("route_build", route_build_launches(self.n, E),
+             lambda: p.moe_route_build(self.idx, E, r.pad_multiple, workspace=self.ws, out=rt)),
             ("binned_gather", 1, lambda: p.moe_binned_gather(self.x, rt.indices, rt.bins, E, r.capacity, K,
                                                              out=self.xb, positions=rt.positions)),
             ("binned_scatter", 1, lambda: p.moe_binned_scatter(self.xb, rt.indices, rt.bin_ids, rt.bins, w, T, K,

@@ -48,17 +48,42 @@ def source_digest() -> str:
     return h.hexdigest()[:16]
 
 
+def _code_only(text: str) -> str:
+    """C/C++ source with comments removed and whitespace runs collapsed
+    (string and character literals kept as they are)."""
+    out, i, n = [], 0, len(text)
+    while i < n:
+        c = text[i]
+        if text.startswith("//", i):
+            j = text.find("\n", i)
+            i = n if j < 0 else j
+        elif text.startswith("/*", i):
+            j = text.find("*/", i + 2)
+            i = n if j < 0 else j + 2
+            out.append(" ")
+        elif c in "\"'":
+            j = i + 1
+            while j < n and text[j] != c:
+                j += 2 if text[j] == "\\" else 1
+            out.append(text[i:j + 1])
+            i = j + 1
+        else:
+            out.append(c)
+            i += 1
+    return " ".join("".join(out).split())
+
+
 def kernel_digest(unit: str) -> str:
     """Hash of one kernel family's translation unit (``csrc/<unit>.cu``), the
-    shared headers and the compile flags: it changes only when what that
-    kernel is compiled from changes, so a profile taken on it stays valid
-    while other kernels are edited."""
+    shared headers and the compile flags, comments and layout left out: it
+    changes only when what that kernel is compiled from changes, so a profile
+    taken on it stays valid while other kernels, or comments, are edited."""
     h = hashlib.sha256()
     files = [os.path.join(CSRC, unit + ".cu")] + sorted(glob.glob(os.path.join(CSRC, "*.cuh")))
     for f in files:
         h.update(os.path.basename(f).encode())
-        with open(f, "rb") as fh:
-            h.update(fh.read())
+        with open(f, encoding="utf-8") as fh:
+            h.update(_code_only(fh.read()).encode())
     h.update(" ".join(ARCH + NVCC_FLAGS[:-4]).encode())
     return h.hexdigest()[:16]
 

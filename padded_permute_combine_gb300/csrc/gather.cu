@@ -11,7 +11,8 @@
 //    reads a token row once and writes it to each of the token's kept
 //    output rows, so x leaves HBM once instead of once per kept slot;
 //  - destination-major (gather_kernel; tiny outputs, and the last few rows
-//    of the token-major schedule): one warp owns one output row, finds its
+//    of the token-major schedule when it has to build the positions in the
+//    output's tail): one warp owns one output row, finds its
 //    source assignment through bins and indices (a padded row finds its
 //    expert by binary search over padded_bins) and streams the row; token
 //    rows are loaded evict-last there, as up to TOP_K rows copy the same
@@ -180,13 +181,17 @@ __global__ void __launch_bounds__(kThreads) gather_kernel(GatherArgs g) {
 
 // ------------------------------------------------------- token-major path
 //
-// When the output is larger than n int32 values (every realistic shape), the
-// gather reads each token row once: (1) the inverse permutation of indices is
-// written into the last bytes of `out` itself, so no workspace is needed;
-// (2) one warp per token resolves the token's TOP_K slots to output rows
-// through it and copies the token row to every kept row, and the same launch
-// zero-fills the unused rows; (3) the few rows that overlap the borrowed
-// tail are then produced destination-major by gather_kernel, overwriting it.
+// The gather reads each token row once. One warp per token resolves the
+// token's TOP_K slots to output rows through the inverse permutation of
+// indices (positions[a] = sorted position of assignment a, checked against
+// indices before it is followed) and copies the token row to every kept
+// row, and the same launch zero-fills the unused rows. The positions come
+// from the caller (the route build writes them): one launch. Without them,
+// when the output is larger than n int32 values (every realistic shape),
+// (1) the inverse permutation is first written into the last bytes of `out`
+// itself, so no workspace is needed, (2) the token pass runs on it, and
+// (3) the few rows that overlap that borrowed tail are then produced
+// destination-major by gather_kernel, overwriting it.
 
 __global__ void positions_kernel(const int32_t* __restrict__ indices, int64_t n, int32_t* __restrict__ positions,
                                  int32_t* status) {

@@ -371,7 +371,8 @@ gather_token_kernel(GatherArgs g) {
 // the copies: per row chunk, lane 0 of a warp issues one bulk load of the
 // token row chunk into shared memory (completion tracked by an mbarrier)
 // and one bulk store of it to each kept output row; zero rows are bulk
-// stores of a zeroed chunk. One instruction moves up to kTmaChunk bytes, so
+// stores of a zeroed chunk (binned: by the same warps after their token
+// segments; padded: by extra warps of the CTA that do nothing else). One instruction moves up to kTmaChunk bytes, so
 // the load/store units are no longer the limit (the register path issues
 // one 32-byte store per lane per vector and stalls on their queue). Each
 // warp alternates two chunk buffers, so a chunk's load overlaps the
@@ -391,7 +392,15 @@ gather_token_kernel(GatherArgs g) {
 #define MOE_TMA_WARPS 4
 #endif
 constexpr int kTmaWarps = MOE_TMA_WARPS;
-constexpr int kTmaThreads = kTmaWarps * kWarp;
+// Padded outputs: 4 more warps per CTA only zero-fill the padding rows,
+// concurrently with the copy warps (0.230 -> 0.224 ms at the DeepSeek-V3
+// batch). Binned outputs measured faster with the copy warps zero-filling
+// after their token segments (no extra warps).
+constexpr int kPaddedZeroWarps = 4;
+template <bool PADDED>
+__host__ __device__ constexpr int zero_warps() { return PADDED ? kPaddedZeroWarps : 0; }
+template <bool PADDED>
+__host__ __device__ constexpr int tma_threads() { return (kTmaWarps + zero_warps<PADDED>()) * kWarp; }
 #ifndef MOE_TMA_CHUNK
 #define MOE_TMA_CHUNK 8192
 #endif
@@ -399,7 +408,7 @@ constexpr int kTmaChunk = MOE_TMA_CHUNK;  // bytes per staged row chunk
 constexpr size_t kTmaSmem = (size_t)kTmaChunk * (1 + 2 * kTmaWarps) + 16 * kTmaWarps;
 
 template <bool PADDED>
-__global__ void __launch_bounds__(kTmaThreads, 1) gather_tma_kernel(GatherArgs g, int64_t row_bytes) {
+__global__ void __launch_bounds__(tma_threads<PADDED>(), 1) gather_tma_kernel(GatherArgs g, int64_t row_bytes) {
   await_previous_kernel();
   constexpr unsigned kAll = 0xffffffffu;
   extern __shared__ __align__(128) unsigned char tsm[];
@@ -407,10 +416,12 @@ __global__ void __launch_bounds__(kTmaThreads, 1) gather_tma_kernel(GatherArgs g
   __shared__ int32_t spbins[PADDED ? kStageMax : 1];
   const int warp = threadIdx.x / kWarp, lane = lane_id();
   unsigned char* zero = tsm;
-  unsigned char* bufs = tsm + (size_t)kTmaChunk * (1 + 2 * warp);
-  uint64_t* bars = reinterpret_cast<uint64_t*>(tsm + (size_t)kTmaChunk * (1 + 2 * kTmaWarps)) + 2 * warp;
+  constexpr int kZeroWarps = zero_warps<PADDED>();
+  const bool copier = warp < kTmaWarps;
+  unsigned char* bufs = tsm + (size_t)kTmaChunk * (1 + 2 * (copier ? warp : 0));
+  uint64_t* bars = reinterpret_cast<uint64_t*>(tsm + (size_t)kTmaChunk * (1 + 2 * kTmaWarps)) + 2 * (copier ? warp : 0);
   for (int q = threadIdx.x; q < kTmaChunk / 16; q += blockDim.x) reinterpret_cast<uint4*>(zero)[q] = make_uint4(0, 0, 0, 0);
-  if (lane == 0) {
+  if (lane == 0 && copier) {
     mbar_init(smem_u32(bars));
     mbar_init(smem_u32(bars + 1));
   }
@@ -436,27 +447,30 @@ __global__ void __launch_bounds__(kTmaThreads, 1) gather_tma_kernel(GatherArgs g
     if (PADDED && threadIdx.x == 0 && spb[g.E - 1] > g.rows_out) flag_status(g.status, MOE_STATUS_ROWS_MISMATCH);
   }
 
+  if (kZeroWarps > 0 && !copier) {
+    // Zero-fill warps: candidate rows below row_begin, strided over the
+    // grid's zero warps, concurrently with the copy warps' token segments.
+    const int64_t zwarps = (int64_t)gridDim.x * kZeroWarps;
+    for (int64_t r = (int64_t)blockIdx.x * kZeroWarps + (warp - kTmaWarps); r < g.row_begin; r += zwarps) {
+      if (lane == 0 && is_zero_row<PADDED>(g, sb, spb, r)) {
+        for (int64_t off = 0; off < row_bytes; off += kTmaChunk)
+          bulk_store(g.out + r * row_bytes + off, smem_u32(zero), (uint32_t)min((int64_t)kTmaChunk, row_bytes - off));
+        bulk_commit();
+      }
+    }
+    if (lane == 0) bulk_wait_all();  // the stores have read the zero chunk
+    return;
+  }
   const int64_t warps = (int64_t)gridDim.x * kTmaWarps;
   const int64_t token_items = g.T * g.segs;
-  const int64_t items = token_items + g.row_begin;  // token segments, then the rows this kernel may zero-fill
+  // token segments, then (unless zero warps do them) the rows this kernel may zero-fill
+  const int64_t items = token_items + (kZeroWarps > 0 ? 0 : g.row_begin);
   uint32_t parity = 0;                       // bit b: parity of buffer b's next completion
   int use = 0;                               // buffer of the next chunk
   bool ok = true;
   for (int64_t item = (int64_t)blockIdx.x * kTmaWarps + warp; item < items && ok; item += warps) {
-    int64_t titem = item, r = item - token_items;
-    bool token = item < token_items;
-    if (PADDED) {
-      // Padded: token segments and candidate zero rows mixed evenly along
-      // the item order, so the checks of the many candidate rows that are
-      // not padding (a binary search each) overlap the copies instead of
-      // forming a tail of their own. (Binned rows measured faster with all
-      // token segments first.)
-      const int64_t before = item * token_items / items, upto = (item + 1) * token_items / items;
-      token = upto > before;
-      titem = before;
-      r = item - before;
-    }
-    if (!token) {
+    if (item >= token_items) {
+      const int64_t r = item - token_items;
       if (lane == 0 && is_zero_row<PADDED>(g, sb, spb, r)) {
         for (int64_t off = 0; off < row_bytes; off += kTmaChunk)
           bulk_store(g.out + r * row_bytes + off, smem_u32(zero), (uint32_t)min((int64_t)kTmaChunk, row_bytes - off));
@@ -464,8 +478,8 @@ __global__ void __launch_bounds__(kTmaThreads, 1) gather_tma_kernel(GatherArgs g
       }
       continue;
     }
-    const int64_t t = titem / g.segs;
-    const int64_t b_begin = (titem - t * g.segs) * g.seg_len;
+    const int64_t t = item / g.segs;
+    const int64_t b_begin = (item - t * g.segs) * g.seg_len;
     const int64_t b_end = min(b_begin + g.seg_len, row_bytes);
     for (int k0 = 0; k0 < g.top_k && ok; k0 += kWarp) {
       const int64_t a = t * g.top_k + k0 + lane;
@@ -533,7 +547,8 @@ bool launch_gather_tma(const GatherArgs& g, int64_t row_bytes, cudaStream_t s, i
   gt.seg_len = ((row_bytes + gt.segs - 1) / gt.segs + 15) / 16 * 16;  // bytes, 16-byte multiples
   gt.segs = (row_bytes + gt.seg_len - 1) / gt.seg_len;
   const int64_t work_ctas = (gt.T * gt.segs + gt.row_begin + kTmaWarps - 1) / kTmaWarps;
-  launch(k, persistent_grid(k, kTmaThreads, kTmaSmem, work_ctas), kTmaThreads, kTmaSmem, s, gt, row_bytes);
+  launch(k, persistent_grid(k, tma_threads<PADDED>(), kTmaSmem, work_ctas), tma_threads<PADDED>(), kTmaSmem, s, gt,
+         row_bytes);
   *rc = check_launch();
   return true;
 }

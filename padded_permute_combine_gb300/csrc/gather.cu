@@ -396,7 +396,7 @@ constexpr int kTmaWarps = MOE_TMA_WARPS;
 // concurrently with the copy warps (0.230 -> 0.224 ms at the DeepSeek-V3
 // batch). Binned outputs measured faster with the copy warps zero-filling
 // after their token segments (no extra warps).
-constexpr int kPaddedZeroWarps = 4;
+constexpr int kPaddedZeroWarps = 4;  // 1 / 2 / 8 measured 0.256 / 0.222 / 0.229 ms vs 0.222
 template <bool PADDED>
 __host__ __device__ constexpr int zero_warps() { return PADDED ? kPaddedZeroWarps : 0; }
 template <bool PADDED>

@@ -10,13 +10,15 @@ The expert FFN between gather and scatter is the identity (it is not part of
 the routing path), so scatter combines the gathered rows themselves.
 
 Prints one JSON line. ``value`` = routed assignments (rows) per second over
-the whole step, inputs resident in HBM, L2 flushed (512 MB write) before
-every step. ``e2e`` = the same metric through the public API with pinned
+the whole step, inputs resident in HBM, L2 flushed (512 MB written, then
+read back in place) before every step. ``e2e`` = the same metric through the public API with pinned
 host buffers: host->device copies of the inputs and device->host copies of
 the combined outputs and the dense router gradient inside the timed region.
 ``roofline`` reports the dominant kernel against the measured HBM copy
-bandwidth. ``cpu_baseline`` times the CPU oracle on a token subset of the
-same workload on one host core.
+bandwidth. ``cpu_baseline`` times the CPU oracle on one host core over the
+leading tokens of the same workload (as many as one pass covers in half
+its time budget, capped at the whole batch), as many passes as fit in the
+budget.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 """

@@ -298,6 +298,33 @@ def test_more_experts_than_staged_bins(E):
     run_fused(r)
 
 
+def random_routing(seed: int) -> wl.Routing:
+    """A seeded random shape and routing: sizes that straddle the kernels'
+    tiles and limits (16-byte rows or not, the 1024-expert stage, TOP_K up to
+    40, capacity from 0 past the largest count, padding multiples 1..64),
+    distinct or repeated expert choices, uniform or Zipf popularity."""
+    g = np.random.default_rng([seed, 97])
+    dtype = wl.BF16 if g.random() < 0.6 else wl.F32
+    T = int(g.integers(1, 400))
+    H = int(g.choice([int(g.integers(1, 64)), 8 * int(g.integers(1, 140)), 7168 if g.random() < 0.1 else 256]))
+    E = int(g.choice([int(g.integers(1, 20)), int(g.integers(20, 300)), int(g.integers(1000, 1100))]))
+    K = int(g.integers(1, min(E, 10) + 1)) if g.random() < 0.8 else int(g.integers(1, 41))
+    mean = max(1, T * K // E)
+    capacity = int(g.integers(0, 2 * mean + 3))
+    m = int(g.choice([1, 2, 3, 8, 16, 64]))
+    name = "fuzz%d" % seed
+    if g.random() < 0.5 and K <= E:
+        return wl.zipf_routing(name, T, H, E, K, dtype, capacity=capacity, pad_multiple=m, seed=seed)
+    return wl.uniform_routing(name, T, H, E, K, dtype, capacity=capacity, pad_multiple=m,
+                              distinct=K <= E and g.random() < 0.7, seed=seed)
+
+
+@pytest.mark.parametrize("seed", range(40))
+def test_random_shapes(seed):
+    r = random_routing(seed)
+    run_routing(r)
+
+
 def test_no_tokens():
     E = 5
     te = torch.zeros(0, dtype=torch.int32, device=DEV)

@@ -378,6 +378,21 @@ def test_qwen2_moe_57b_compaction():
     run_compaction(wl.qwen2_moe_57b())
 
 
+@pytest.mark.parametrize("seed", range(20))
+def test_compaction_random_shapes(seed):
+    # Maps of 1 to 3000 experts (multiples of 4 and 16 or not: the staged,
+    # row-per-thread, warp and chunk kernels), topk up to 12, rows with more
+    # routes than topk, up to 900 rows (blocks of consecutive rows that end
+    # short of T).
+    g = np.random.default_rng([seed, 131])
+    E = int(g.choice([int(g.integers(1, 70)), 4 * int(g.integers(1, 520)), 16 * int(g.integers(1, 130)),
+                      int(g.integers(2049, 3000))]))
+    topk = int(g.integers(1, 13))
+    T = int(g.integers(1, 900))
+    run_compaction(wl.dense_routes("crand%d" % seed, T, E, topk, max_routes=min(E, topk + int(g.integers(0, 5))),
+                                   seed=seed))
+
+
 @pytest.mark.parametrize("T,E,topk,max_routes", [(1, 1, 1, 1), (333, 5, 3, 5), (1000, 64, 8, 12), (257, 160, 6, 6),
                                                  (100, 37, 40, 37), (513, 256, 8, 8), (777, 48, 5, 9),
                                                  (300, 16, 8, 16), (65, 32, 2, 32)])

@@ -26,6 +26,7 @@
 #include "vec_math.cuh"
 #include "bulk.cuh"
 
+#include <atomic>
 #include <type_traits>
 
 namespace moe {
@@ -532,15 +533,19 @@ template <bool PADDED>
 bool launch_gather_tma(const GatherArgs& g, int64_t row_bytes, cudaStream_t s, int* rc) {
   if (!MOE_GATHER_TMA || row_bytes % 16 != 0 || !aligned(g.x, 16) || !aligned(g.out, 16)) return false;
   auto k = gather_tma_kernel<PADDED>;
-  static int configured[64] = {0};
+  // The dynamic shared-memory opt-in is per device; set it once per device
+  // (concurrent callers may both set it, which is harmless).
+  constexpr int kMaxDevices = 64;
+  static std::atomic<int> configured[kMaxDevices];
   int dev = 0;
   (void)cudaGetDevice(&dev);
-  if (dev < 0 || dev >= 64 || !configured[dev]) {
+  const bool cached = dev >= 0 && dev < kMaxDevices;
+  if (!cached || configured[dev].load(std::memory_order_relaxed) == 0) {
     if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kTmaSmem) != cudaSuccess) {
       (void)cudaGetLastError();
       return false;
     }
-    if (dev >= 0 && dev < 64) configured[dev] = 1;
+    if (cached) configured[dev].store(1, std::memory_order_relaxed);
   }
   GatherArgs gt = g;
   gt.segs = MOE_TMA_SEGS;

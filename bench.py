@@ -116,9 +116,9 @@ def traffic_from_profiles(kernel: str, digest: str):
 def route_build_launches(n: int, E: int) -> int:
     """Kernels one moe_route_build launches: hist, scan, scatter; the scan
     folds into the scatter pass when chunks x experts <= 16384 and E <= 256
-    (chunks of 2048 assignments for E <= 768)."""
+    (chunks of 1024 assignments for E <= 768)."""
     warps = max(1, min(16, (48 * 1024) // (4 * E)))
-    chunks = max(1, -(-n // (warps * 32 * 4)))
+    chunks = max(1, -(-n // (warps * 32 * 2)))
     return 2 if (n > 0 and E <= 256 and chunks * E <= 16384) else 3
 
 

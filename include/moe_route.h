@@ -128,7 +128,7 @@ int moe_route_build(const int32_t* top_expert, int64_t n, int32_t num_experts,
  *  - Size limit: returns MOE_ERR_INVALID_ARG, without enqueuing anything,
  *    when moe_route_build_workspace_size(n, num_experts) exceeds
  *    MOE_ROUTE_BUILD_NOALLOC_MAX_BYTES (for E = 256 that is n above about
- *    two million assignments); use moe_route_build with a caller workspace
+ *    one million assignments); use moe_route_build with a caller workspace
  *    then.
  *  - The first call on a device looks up the array's device address
  *    (cudaGetSymbolAddress) and caches it; make that first call before any

@@ -19,9 +19,12 @@
 namespace moe {
 namespace {
 
-// Chunks of 16 warps x 4 rounds (2048 assignments) measured fastest at the
-// DeepSeek-V3 size; smaller chunks give more CTAs but a longer scan.
-constexpr int kRounds = 4;      // 32-element rounds per warp and chunk
+// Chunks of 16 warps x 2 rounds (1024 assignments): 64 CTAs at the
+// DeepSeek-V3 size (65 536 assignments), whose 64 x 256 count matrix each
+// scatter CTA can read to derive its own prefixes. 4 rounds (32 CTAs) took
+// 15.9 us, 2 rounds 14.7 us, 1 round (128 CTAs, too many counts for the
+// fused scan, so three launches) 17.5 us.
+constexpr int kRounds = 2;      // 32-element rounds per warp and chunk
 constexpr int kMaxWarps = 16;   // warps per CTA of the hist / scatter passes
 constexpr int kSmemBudget = 48 * 1024;  // per-warp counters of the scatter pass
 constexpr int kScanThreads = 1024;

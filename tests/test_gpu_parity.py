@@ -343,12 +343,12 @@ def test_misaligned_pointers_take_narrow_vectors():
 
 
 def test_large_route_build_many_chunks():
-    # Both schedules: the scan folded into the scatter pass (chunks of 2048 x
-    # E <= 16384 and E <= 256: 131 072 x 256 is the last such shape, 65 536 x
+    # Both schedules: the scan folded into the scatter pass (chunks of 1024 x
+    # E <= 16384 and E <= 256: 65 536 x 256 is the last such shape, 65 536 x
     # 1, 30 000 x 256) and the separate scan (one more assignment, E = 257,
     # and the larger shapes).
     g = np.random.default_rng(11)
-    for n, E in [(200_003, 256), (70_001, 4096), (65_536, 1), (131_072, 3000), (131_072, 256), (131_073, 256),
+    for n, E in [(200_003, 256), (70_001, 4096), (65_536, 1), (131_072, 3000), (65_536, 256), (65_537, 256),
                  (30_000, 256), (30_000, 257)]:
         te = g.integers(0, E, size=n).astype(np.int32)
         route = p.moe_route_build(to_dev(te, DEV), E, 128)

@@ -232,4 +232,17 @@ int persistent_grid(Kernel k, int threads, size_t smem, int64_t work_ctas) {
   return (int)(g < 1 ? 1 : g);
 }
 
+// Grid for a grid-stride kernel whose warps each take about `items_per_warp`
+// items: ceil(work_ctas / items_per_warp) CTAs (work_ctas = CTAs at one item
+// per warp), more than fit at once, so the block scheduler hands the later
+// CTAs to whichever SMs free up first and uneven item costs even out across
+// SMs. items_per_warp <= 0 gives the persistent grid.
+template <typename Kernel>
+int balanced_grid(Kernel k, int threads, size_t smem, int64_t work_ctas, int items_per_warp) {
+  if (items_per_warp <= 0) return persistent_grid(k, threads, smem, work_ctas);
+  int64_t g = (work_ctas + items_per_warp - 1) / items_per_warp;
+  if (g > 0x7fffffff) g = 0x7fffffff;
+  return (int)(g < 1 ? 1 : g);
+}
+
 }  // namespace moe

@@ -463,14 +463,15 @@ __global__ void __launch_bounds__(kThreads, 4) wgrad_kept_kernel(WgradArgs g) {
 #ifndef MOE_WGRAD_KEPT
 #define MOE_WGRAD_KEPT 1
 #endif
-// Items per warp of the slot-walk grid (0: persistent grid). One: a CTA per
-// eight slots, balanced across SMs by the block scheduler (padded
-// DeepSeek-V3 batch 0.1766 -> 0.1738 ms). The kept-row walk stays
+// Items per warp of the slot-walk grid (0: persistent grid). Two: a CTA per
+// sixteen slots, balanced across SMs by the block scheduler (padded
+// DeepSeek-V3 batch 0.1766 persistent, 0.1738 at one item per warp, 0.1725
+// at two). The kept-row walk stays
 // persistent (0.102 -> 0.127 ms with a CTA per eight slots): each of its
 // CTAs first stages the bins and the phase prefixes, and its phases keep
 // the gradient rows in L2 only while all warps sweep them together.
 #ifndef MOE_WGRAD_ITEMS
-#define MOE_WGRAD_ITEMS 1
+#define MOE_WGRAD_ITEMS 2
 #endif
 
 template <int VB, typename ET, bool PADDED>

@@ -399,8 +399,9 @@ __global__ void invert_kernel(const int32_t* __restrict__ indices, int64_t n, in
 // Items per warp of the asynchronous scatter's grid (0: persistent grid).
 // One: a CTA per four token segments, so the block scheduler gives the
 // later CTAs to the SMs that finish first and tokens' uneven kept counts
-// even out across SMs (DeepSeek-V3 batch: binned 0.0966 -> 0.0938 ms,
-// padded 0.1766 -> 0.1693; two items per warp 0.0942 / 0.1697).
+// even out across SMs (DeepSeek-V3 batch, items of 224 vectors: binned
+// 0.0966 -> 0.0938 ms, padded 0.1766 -> 0.1693; two items per warp
+// 0.0942 / 0.1697).
 #ifndef MOE_SCATTER_ITEMS
 #define MOE_SCATTER_ITEMS 1
 #endif

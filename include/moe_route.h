@@ -133,7 +133,10 @@ int moe_route_build(const int32_t* top_expert, int64_t n, int32_t num_experts,
  *  - The first call on a device looks up the array's device address
  *    (cudaGetSymbolAddress) and caches it; make that first call before any
  *    stream capture on that device. It returns MOE_ERR_CUDA if the lookup
- *    fails.
+ *    fails. The cached address is kept for the life of the process: after a
+ *    cudaDeviceReset the library's device image is loaded again and the
+ *    array may move, so do not call this entry point on a device that has
+ *    been reset since its first call.
  *  - All calls on a device share the one array, which keeps the last call's
  *    contents (nothing in it needs to start at zero). Calls whose work
  *    overlaps on the GPU - on different streams without ordering between
@@ -297,7 +300,10 @@ int moe_route_build_padded_gather(const int32_t* top_expert, const void* x,
  *   positions [n] nullable: the inverse permutation from moe_route_build.
  *   When NULL it is rebuilt in `workspace`
  *   (>= moe_scatter_workspace_size(n) bytes); otherwise workspace may be
- *   NULL.
+ *   NULL. Every entry is checked against indices before it is followed
+ *   (indices[positions[a]] must equal a): a positions vector from another
+ *   routing, or one with entries exchanged, sets MOE_STATUS_BAD_INDEX in
+ *   d_status and the mismatched slots contribute nothing.
  */
 size_t moe_scatter_workspace_size(int64_t n);
 int moe_binned_scatter(const void* xe, int32_t dtype, const int32_t* indices,

@@ -43,14 +43,20 @@ struct ScatterArgs {
   int32_t capacity;
   int32_t top_k;
   int32_t* status;
+  const int32_t* indices = nullptr;  // checked against positions before a slot is followed
 };
 
 // Row of the expert tensor holding assignment a, or -1 when it was dropped.
+// The positions entry is checked against indices (indices[positions[a]] must
+// be a), so positions left over from another routing are flagged, never
+// followed.
 template <bool PADDED>
 __device__ __forceinline__ int64_t slot_row(const ScatterArgs& g, int64_t a) {
   const int32_t i = __ldg(g.positions + a);
   if (i < 0 || i >= g.n) { flag_status(g.status, MOE_STATUS_BAD_INDEX); return -1; }
+  const int32_t back = __ldg(g.indices + i);  // issued together with the bin_ids load
   const int32_t e = __ldg(g.bin_ids + i);
+  if (back != a) { flag_status(g.status, MOE_STATUS_BAD_INDEX); return -1; }
   if (e < 0 || e >= g.E) { flag_status(g.status, MOE_STATUS_BAD_EXPERT); return -1; }
   const int64_t start = e > 0 ? __ldg(g.bins + e - 1) : 0;
   const int64_t j = i - start;
@@ -446,6 +452,7 @@ int run_scatter(ScatterArgs g, int32_t dtype, const int32_t* indices, void* work
   const int vb = pick_vec_bytes(row_bytes, ptrs, 2, eb);
   if (vb == 0) return MOE_ERR_UNSUPPORTED;
   g.vecs = row_bytes / vb;
+  g.indices = indices;
   if (g.positions == nullptr && g.n > 0) {
     if (workspace == nullptr || ws_bytes < moe_scatter_workspace_size(g.n) || !aligned(workspace, 4))
       return MOE_ERR_INVALID_ARG;

@@ -503,6 +503,48 @@ def test_corrupt_bins_and_positions_are_reported():
     assert int(st.item()) & _lib.MOE_STATUS_ROWS_MISMATCH
 
 
+@pytest.mark.parametrize("dtype", [wl.F32, wl.BF16])
+def test_scatter_flags_swapped_positions(dtype):
+    """A valid route's positions with two entries exchanged (every entry in
+    range, the vector still a permutation) sets MOE_STATUS_BAD_INDEX in both
+    scatters, and neither misrouted slot reaches the output: each token equals
+    the oracle's combine with those two slots left out (weight 0, which adds a
+    signed zero and so leaves the fp32 sum unchanged)."""
+    r = wl.uniform_routing("swapped", 48, 40, 6, 3, dtype, capacity=20, pad_multiple=4, seed=31)
+    T, H, E, K = r.T, r.H, r.E, r.K
+    n = T * K
+    o = oracle.route_build(r.top_expert, E, r.pad_multiple)
+    route = p.moe_route_build(to_dev(r.top_expert, DEV), E, r.pad_multiple)
+    a1, a2 = 1, n - 2  # slots of different tokens
+    pos = o["positions"].copy()
+    pos[a1], pos[a2] = pos[a2], pos[a1]
+    bad_pos = to_dev(pos, DEV)
+    w_cut = r.weights.reshape(-1).copy()
+    w_cut[[a1, a2]] = 0.0
+    ones_cut = np.ones(n, np.float32)
+    ones_cut[[a1, a2]] = 0.0
+    w = to_dev(r.weights.reshape(-1), DEV)
+    P = int(o["padded_bins"][-1])
+    xb_np = wl.expert_rows(E * r.capacity, H, dtype, 5).reshape(E, r.capacity, H)
+    xp_np = wl.expert_rows(P, H, dtype, 6)
+    xb, xp = to_dev(xb_np, DEV), to_dev(xp_np, DEV)
+    for weights, o_w, tag in ((w, w_cut, "weighted"), (None, ones_cut, "unweighted")):
+        st = status_word()
+        y = p.moe_binned_scatter(xb, route.indices, route.bin_ids, route.bins, weights, T, K, positions=bad_pos,
+                                 status=st)
+        torch.cuda.synchronize()
+        assert int(st.item()) == _lib.MOE_STATUS_BAD_INDEX, tag
+        want = oracle.binned_scatter(xb_np, o["indices"], o["bin_ids"], o["bins"], o_w, T, K)
+        assert_bits_equal(to_host(y), want, "binned scatter, swapped positions, " + tag)
+        st.zero_()
+        y = p.moe_padded_scatter(xp, route.indices, route.bin_ids, route.bins, route.padded_bins, weights, T, K,
+                                 positions=bad_pos, status=st)
+        torch.cuda.synchronize()
+        assert int(st.item()) == _lib.MOE_STATUS_BAD_INDEX, tag
+        want = oracle.padded_scatter(xp_np, o["indices"], o["bin_ids"], o["bins"], o["padded_bins"], o_w, T, K)
+        assert_bits_equal(to_host(y), want, "padded scatter, swapped positions, " + tag)
+
+
 def test_compaction_bwd_bad_index_reported():
     idx = torch.tensor([[0, 7], [1, -1]], dtype=torch.int32, device=DEV)
     g = torch.tensor([[1.0, 2.0], [3.0, 4.0]], device=DEV)

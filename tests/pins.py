@@ -152,6 +152,58 @@ def check_roundtrip_kx(lib):
             assert np.array_equal(oracle.to_f32(y), K * xf)
 
 
+def check_scatter_slot_order(lib):
+    """The combine adds a token's TOP_K slots in fp32 one after the other, k
+    ascending from +0.0: the hand-worked non-associative example of
+    tests/golden/scatter_slot_order.txt, binned (capacity 1) and padded
+    (multiple 1), unweighted and with unit weights, fp32 and bf16 rows."""
+    d = read_golden("scatter_slot_order.txt")
+    te = np.array(d["top_expert"], np.int32).reshape(-1)
+    K, E = d["top_k"], d["num_experts"]
+    T = te.size // K
+    xe = np.array(d["xe"], np.float32)
+    want = d["scatter"]
+    r = oracle.route_build(te, E, 1, lib=lib)
+    for rows in (xe, oracle.f32_to_bf16(xe, lib=lib)):
+        for w in (None, np.ones(te.size, np.float32)):
+            y = oracle.binned_scatter(rows.reshape(E, 1, -1), r["indices"], r["bin_ids"], r["bins"], w, T, K, lib=lib)
+            assert oracle.to_f32(y).tolist() == want
+            y = oracle.padded_scatter(rows, r["indices"], r["bin_ids"], r["bins"], r["padded_bins"], w, T, K, lib=lib)
+            assert oracle.to_f32(y).tolist() == want
+
+
+def check_scatter_sequential(lib):
+    """On values that do not associate in fp32 (signed powers of two from
+    2^-12 to 2^24 times small odd integers), the unweighted combine of every
+    token equals numpy's sequential fp32 accumulation (np.cumsum with a
+    float32 accumulator) over a +0.0 start followed by the token's kept slots
+    in slot order, each slot's row taken from the sort-free definition of
+    where an assignment lands."""
+    g = _rng(21)
+    for te, E, K in _routings():
+        n = te.size
+        T = n // K
+        H = 6
+        r = oracle.route_build(te, E, 1, lib=lib)
+        for cap in (1, 2, max(1, n)):
+            rows = _ref_rows(te, E, K, cap=cap)
+            xe = (g.choice([-1.0, 1.0], size=(E * cap, H)) * np.exp2(g.integers(-12, 25, size=(E * cap, H)))
+                  * g.choice([1.0, 3.0, 5.0], size=(E * cap, H))).astype(np.float32)
+            y = oracle.binned_scatter(xe.reshape(E, cap, H), r["indices"], r["bin_ids"], r["bins"], None, T, K,
+                                      lib=lib)
+            for t in range(T):
+                terms = [np.zeros(H, np.float32)] + [xe[rows[t * K + k]] for k in range(K) if rows[t * K + k] >= 0]
+                want = np.cumsum(np.stack(terms), axis=0, dtype=np.float32)[-1]
+                assert np.array_equal(y[t].view(np.uint32), want.view(np.uint32))
+        prow = _ref_rows(te, E, K, m=1)
+        xp = (g.choice([-1.0, 1.0], size=(n, H)) * np.exp2(g.integers(-12, 25, size=(n, H)))).astype(np.float32)
+        y = oracle.padded_scatter(xp, r["indices"], r["bin_ids"], r["bins"], r["padded_bins"], None, T, K, lib=lib)
+        for t in range(T):
+            terms = [np.zeros(H, np.float32)] + [xp[prow[t * K + k]] for k in range(K)]
+            want = np.cumsum(np.stack(terms), axis=0, dtype=np.float32)[-1]
+            assert np.array_equal(y[t].view(np.uint32), want.view(np.uint32))
+
+
 def check_adjoint(lib):
     """<gather(x), Y> == <x, scatter_unweighted(Y)> for binned and padded,
     and <fwd(p), G> == <p, bwd(G)> for the compaction, on integer data where
@@ -575,6 +627,8 @@ ALL_CHECKS = [
     check_route_textbook,
     check_gather_rows,
     check_roundtrip_kx,
+    check_scatter_slot_order,
+    check_scatter_sequential,
     check_adjoint,
     check_weighted_gather,
     check_wgrad_derivative,

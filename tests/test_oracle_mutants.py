@@ -36,6 +36,8 @@ MUTANTS = [
     ("scatter_weight_index", "float scaled = weights[a] * v;", "float scaled = weights[(a + 1) % n] * v;"),
     ("scatter_drop_term", "acc[h] = acc[h] + scaled;", "acc[h] = scaled;"),
     ("scatter_unweighted_drop_term", "acc[h] = acc[h] + v;", "acc[h] = v;"),
+    ("scatter_reversed_slots", "for (int32_t k = 0; k < top_k; ++k) {\n            int64_t a = t * top_k + k;",
+     "for (int32_t k = top_k - 1; k >= 0; --k) {\n            int64_t a = t * top_k + k;"),
     ("scatter_skip_first_slot", "for (int32_t k = 0; k < top_k; ++k) {\n            int64_t a = t * top_k + k;",
      "for (int32_t k = (top_k > 1 ? 1 : 0); k < top_k; ++k) {\n            int64_t a = t * top_k + k;"),
     ("wgrad_token_mod", "int64_t token = indices[i] / top_k;\n        double dot",

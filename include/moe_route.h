@@ -69,7 +69,9 @@ enum moe_device_status {
   MOE_STATUS_BAD_INDEX = 2,    /* an index or position outside its range */
   MOE_STATUS_BAD_BINS = 4,     /* bins / padded_bins not monotonic or not consistent */
   MOE_STATUS_ROWS_MISMATCH = 8, /* padded_bins[E-1] exceeds the rows the caller provided */
-  MOE_STATUS_TIMEOUT = 16       /* a bounded wait on an asynchronous copy gave up; outputs unspecified */
+  MOE_STATUS_TIMEOUT = 16       /* a bounded wait on an asynchronous copy gave up: the launch's
+                                   outputs are unspecified and the stream must be
+                                   treated as failed (a copy may still be landing) */
 };
 
 /* Library limits (inclusive). */

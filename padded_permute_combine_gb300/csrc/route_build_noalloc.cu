@@ -12,7 +12,8 @@
 // library is loaded keeps these bytes reserved until the process exits. On
 // each device, the first call looks up the array's device address with
 // cudaGetSymbolAddress (host code cannot use the array's name as a device
-// pointer) and caches it.
+// pointer) and caches it for the life of the process; a device reset, after
+// which the array may live elsewhere, is not detected (the header says so).
 #include <mutex>
 
 #include "common.cuh"

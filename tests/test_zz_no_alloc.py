@@ -35,8 +35,12 @@ def test_noalloc_route_build_matches_workspace_route_build():
     dev = torch.device("cuda:0")
     stream = torch.cuda.current_stream(dev).cuda_stream
     g = np.random.default_rng(2024)
-    # large first, then smaller: the second call sees stale scratch contents
-    for n, E, m in [(65536, 256, 128), (5003, 64, 16)]:
+    # Every call starts from the previous call's leftover scratch. 65536 and
+    # 5003 assignments take the two-launch path (the count matrix is small
+    # enough for every scatter CTA to scan it); 300000 assignments at E = 256
+    # (293 chunks, 300 KB of counts) take the three-launch path, whose scan
+    # pass rewrites the counts in place.
+    for n, E, m in [(65536, 256, 128), (300000, 256, 128), (5003, 64, 16)]:
         p = 1.0 / np.arange(1, E + 1) ** 1.1
         te_np = g.choice(E, size=n, p=p / p.sum()).astype(np.int32)
         te = torch.from_numpy(te_np).to(dev)
@@ -54,8 +58,15 @@ def test_noalloc_route_build_matches_workspace_route_build():
         for name, a, b in zip(("indices", "bin_ids", "bins", "padded_bins", "positions"), got, want):
             assert torch.equal(a, b), name
 
-    # more scratch than the fixed array holds: refused on the host
-    big_n = 1 << 22
-    assert lib.moe_route_build_workspace_size(big_n, 256) > (1 << 20)
-    rc = lib.moe_route_build_noalloc(_ptr(te), big_n, 256, 1, *[_ptr(t) for t in got], None, stream)
+    # more scratch than the fixed array holds: refused on the host. The
+    # buffers are sized for the request, so that a call which slipped past
+    # the check would still stay inside them.
+    big_n, big_e = 1 << 22, 256
+    assert lib.moe_route_build_workspace_size(big_n, big_e) > (1 << 20)
+    big_te = torch.zeros(big_n, dtype=torch.int32, device=dev)
+    big = [torch.empty(big_n, dtype=torch.int32, device=dev), torch.empty(big_n, dtype=torch.int32, device=dev),
+           torch.empty(big_e, dtype=torch.int32, device=dev), torch.empty(big_e, dtype=torch.int32, device=dev),
+           torch.empty(big_n, dtype=torch.int32, device=dev)]
+    rc = lib.moe_route_build_noalloc(_ptr(big_te), big_n, big_e, 1, *[_ptr(t) for t in big], None, stream)
     assert rc == _lib.MOE_ERR_INVALID_ARG
+    torch.cuda.synchronize(dev)

@@ -3,9 +3,13 @@
 //
 // Rules every caller keeps: both addresses and the size are multiples of
 // 16 bytes; a load's completion is awaited only through mbar_wait, which
-// gives up after kSpinLimit polls (the caller then flags
-// MOE_STATUS_TIMEOUT, drains what it issued and stops) so no kernel can
-// spin forever on a copy that never lands.
+// gives up after kSpinLimit polls, so no kernel can spin forever on a copy
+// that never lands. The caller then flags MOE_STATUS_TIMEOUT, waits once
+// more (bounded) for its outstanding load, drains its bulk stores
+// (bulk_wait_all covers stores only, not loads) and stops. If the second
+// wait gives up too, the load may still target the CTA's shared memory after
+// the CTA exits: the launch's output and the stream are then undefined and
+// the caller must treat them as failed.
 #pragma once
 
 #include <cstdint>

@@ -378,7 +378,9 @@ gather_token_kernel(GatherArgs g) {
 // one 32-byte store per lane per vector and stalls on their queue). Each
 // warp alternates two chunk buffers, so a chunk's load overlaps the
 // previous chunk's stores. Every mbarrier wait is bounded: after kSpinLimit
-// polls the warp sets MOE_STATUS_TIMEOUT, drains its stores and stops.
+// polls the warp sets MOE_STATUS_TIMEOUT, waits once more (bounded) for the
+// load it issued, drains its stores and stops; the output of that launch is
+// then undefined.
 
 #ifndef MOE_GATHER_TMA
 #define MOE_GATHER_TMA 1
@@ -514,7 +516,11 @@ __global__ void __launch_bounds__(tma_threads<PADDED>(), 1) gather_tma_kernel(Ga
         if (lane == 0) {
           bulk_wait_read_but_one();  // the stores that last read this buffer have finished
           bulk_load(buf, g.x + t * row_bytes + off, bytes, bar);
-          got = mbar_wait(bar, (parity >> use) & 1u);
+          const uint32_t ph = (parity >> use) & 1u;
+          got = mbar_wait(bar, ph);
+          // On a timeout, wait once more (bounded) so that the load does not
+          // land in shared memory after the CTA has gone.
+          if (!got) (void)mbar_wait(bar, ph);
           parity ^= 1u << use;
         }
         ok = __shfl_sync(kAll, (int)got, 0) != 0;

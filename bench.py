@@ -803,15 +803,29 @@ def run_reference(args, rank):
 
 def run_profile_case(args):
     """Each op of a `--tokens`-token batch once as warm-up, then the ops of
-    `--profile-ops` once more. With `ncu -k regex:"gather_kernel|
-    scatter_kernel|wgrad_kernel" -s 8` the captured launches are exactly
-    that second pass (the set-up and warm-up launch eight matching kernels)."""
+    `--profile-ops` once more, in that order, so that an ncu capture with
+    `-k <kernel> -s <launches of that kernel in the warm-up pass>` sees
+    exactly the second pass. Besides the step's ops (and the next rows'
+    `topk_gating`), `qwen_compaction_fwd` / `qwen_compaction_bwd` run the
+    compaction on its own Qwen2-MoE-57B-shaped map (T=65536, E=64, topk=8),
+    once as warm-up and once more when named."""
     import torch
 
     dev = torch.device("cuda", 0)
     r, d = workload(seed=0, tokens=args.tokens)
     path = Path(r, d, dev)
     ops = dict((name, f) for name, _, f in path.ops())
+    logits = torch.from_numpy(wl.normal((r.T, r.E), wl.F32, r.seed, 11)).to(dev)
+    g_out = (torch.empty((r.T, r.K), dtype=torch.int32, device=dev),
+             torch.empty((r.T, r.K), dtype=torch.float32, device=dev))
+    ops["topk_gating"] = lambda: path.p.moe_topk_gating(logits, r.K, "sigmoid", True, out=g_out)
+    q = wl.qwen2_moe_57b()
+    qp, qm, qg = (torch.from_numpy(a).to(dev) for a in (q.probs, q.routing_map, q.grad_probs_indices))
+    qpi = torch.empty((q.probs.shape[0], q.topk), dtype=torch.float32, device=dev)
+    qidx = torch.empty((q.probs.shape[0], q.topk), dtype=torch.int32, device=dev)
+    qgp = torch.empty_like(qp)
+    ops["qwen_compaction_fwd"] = lambda: path.p.moe_routing_map_to_indices_fwd(qp, qm, q.topk, out=(qpi, qidx))
+    ops["qwen_compaction_bwd"] = lambda: path.p.moe_routing_map_to_indices_bwd(qg, qidx, q.probs.shape[1], out=qgp)
     for name in ops:
         ops[name]()
     for name in args.profile_ops.split(","):

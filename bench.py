@@ -3,9 +3,12 @@
 One step = one pass of the whole routing path over one DeepSeek-V3-shaped
 batch (T=8192 tokens, H=7168, E=256 experts, TOP_K=8, capacity 256, padding
 multiple 128, bf16 activations, Zipf(1.1) expert popularity):
-  routing-map compaction -> route build -> binned gather -> binned scatter
-  (weighted) -> binned wgrad -> padded gather -> padded scatter (weighted)
-  -> padded wgrad -> compaction backward.
+  routing-map compaction -> route build -> { binned gather -> binned wgrad
+  -> binned scatter (weighted) } and, on a second stream, { padded gather ->
+  padded wgrad -> padded scatter (weighted) } -> compaction backward.
+The two branches depend only on the route build, so they run concurrently;
+the per-kernel breakdown (`kernels`) times the same ops one after another
+on one stream.
 The expert FFN between gather and scatter is the identity (it is not part of
 the routing path), so scatter combines the gathered rows themselves.
 
@@ -86,7 +89,10 @@ def workload_config(r) -> dict:
             "pad_multiple": r.pad_multiple,
             "l2": "flushed before every step (512 MB write, then read back so no dirty line is left); "
                   "inputs > L2 in total",
-            "expert_ffn": "identity (not part of the routing path)"}
+            "expert_ffn": "identity (not part of the routing path)",
+            "schedule": "compaction -> route build, then the binned branch (gather, wgrad, scatter) and the "
+                        "padded branch (gather, wgrad, scatter) on two streams, joined before the compaction "
+                        "backward; kernels.* are the same ops timed one after another on one stream"}
 
 
 def measured_peak():
@@ -244,6 +250,33 @@ class Path:
                                                                            out=self.gprobs)),
         ]
 
+    def step(self, side):
+        """One step as the dependency graph it is: after the compaction and
+        the route build (on the current stream), the binned branch (gather,
+        wgrad, scatter) runs on the current stream and the padded branch on
+        `side`, concurrently; the compaction backward, which reads the padded
+        wgrad, waits for both. Within a branch the wgrad and the scatter only
+        read the gathered tensor, so their order is free: wgrad first
+        measured fastest (0.850 ms against 0.873 ms with the scatter first,
+        and 0.928 ms for all ops one after another on one stream)."""
+        torch = self.torch
+        named = {name: f for name, _, f in self.ops()}
+        cur = torch.cuda.current_stream(self.dev)
+        named["compaction_fwd"]()
+        named["route_build"]()
+        routed = torch.cuda.Event()
+        routed.record(cur)
+        side.wait_event(routed)
+        with torch.cuda.stream(side):
+            for name in ("padded_gather", "padded_wgrad", "padded_scatter"):
+                named[name]()
+        for name in ("binned_gather", "binned_wgrad", "binned_scatter"):
+            named[name]()
+        joined = torch.cuda.Event()
+        joined.record(side)
+        cur.wait_event(joined)
+        named["compaction_bwd"]()
+
     def next_ops(self):
         """(name, callable, algorithmic bytes) of the rows beyond the routing
         path that are built: router top-k gating (sigmoid, renormalised, on
@@ -399,15 +432,17 @@ def run_gpu(args, rank, world, local_rank):
         if dist is not None:
             dist.barrier()
 
+    side = torch.cuda.Stream(dev)
     for _ in range(args.warmup):
         l2_flush(flush)
-        for _, _, f in ops:
-            f()
+        path.step(side)
     barrier()
 
-    # Whole steps: one event pair around each step and nothing between its
-    # ops, so each kernel's launch overlaps the previous kernel's tail (the
-    # library launches with programmatic stream serialization).
+    # Whole steps: one event pair around each step on the launching stream,
+    # nothing between its ops (each kernel's launch overlaps the previous
+    # kernel's tail: the library launches with programmatic stream
+    # serialization); the padded branch runs on a second stream that joins
+    # the first before the step's last op, so the end event covers it.
     ev_step = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
                for _ in range(args.steps)]
     with ClockSampler(local_rank) as clocks:
@@ -416,14 +451,14 @@ def run_gpu(args, rank, world, local_rank):
         for s in range(args.steps):
             l2_flush(flush)
             ev_step[s][0].record(stream)
-            for _, _, f in ops:
-                f()
+            path.step(side)
             ev_step[s][1].record(stream)
         barrier()
         t_host = time.perf_counter() - t_host
     step_ms = [a.elapsed_time(b) for a, b in ev_step]
     total_ms = max_over_ranks(float(sum(step_ms)), dist, dev)
-    # Per-kernel breakdown: the same steps again with an event after every op.
+    # Per-kernel breakdown: the ops again, one after another on one stream,
+    # with an event after every op.
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(len(ops) + 1)] for _ in range(args.steps)]
     for s in range(args.steps):
         l2_flush(flush)

@@ -509,6 +509,8 @@ def run_gpu(args, rank, world, local_rank):
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": workload_config(r),
         "hbm_gbs_gather_scatter_wgrad": round(hot_bytes / (hot_ms * 1e-3) / 1e9, 1),
+        "step_gbs": round(sum(algo.values()) / (ms_per_step * 1e-3) / 1e9, 1),
+        "step_frac_of_%s_peak" % peak_kind: round(sum(algo.values()) / (ms_per_step * 1e-3) / 1e9 / peak, 4),
         "kernels_ms_sum": round(sum(v["ms"] for v in kern.values()), 5),
         "kernels": kern,
         "roofline": {"bound": "hbm", "kernel": dominant, "achieved": ach, "peak": peak, "peak_kind": peak_kind,

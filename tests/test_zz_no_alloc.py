@@ -6,8 +6,9 @@ whole device memory pool, a hot loop that must not call cudaMalloc).
 moe_route_build_noalloc serves them from a fixed device array inside the
 library. This test calls it through the C ABI twice in a row, on different
 inputs (so the second call starts from the first call's leftover scratch),
-and checks every output against moe_route_build with a caller workspace: the
-outputs are integer index vectors, so they must agree bit for bit. It also
+and checks every output against moe_route_build with a caller workspace and
+against the CPU oracle's route build: the outputs are integer index
+vectors, so they must agree bit for bit. It also
 checks that a request larger than the fixed array is refused before any work
 is enqueued.
 
@@ -19,6 +20,7 @@ import numpy as np
 import pytest
 import torch
 
+import oracle
 from padded_permute_combine_gb300 import _lib, ops
 
 pytestmark = pytest.mark.gpu
@@ -57,6 +59,10 @@ def test_noalloc_route_build_matches_workspace_route_build():
         assert int(status.item()) == 0
         for name, a, b in zip(("indices", "bin_ids", "bins", "padded_bins", "positions"), got, want):
             assert torch.equal(a, b), name
+        # and, independently of the GPU path, the CPU oracle's route build
+        o = oracle.route_build(te_np, E, m)
+        for name, a in zip(("indices", "bin_ids", "bins", "padded_bins", "positions"), got):
+            assert np.array_equal(a.cpu().numpy(), o[name]), name
 
     # more scratch than the fixed array holds: refused on the host. The
     # buffers are sized for the request, so that a call which slipped past

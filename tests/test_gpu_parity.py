@@ -212,6 +212,18 @@ def run_fused(r: wl.Routing, binned=True, padded=True, misalign=False):
         got = to_host(xp)
         assert_bits_equal(got[:P], o_xp, r.name + " fused padded_gather")
         assert not got[P:].any(), r.name + " fused padded_gather rows past padded_bins[-1] not zero"
+        # the combine and the wgrad on that oversized expert tensor (as a caller
+        # that sizes it by the bound does), against the oracle on its first P rows
+        T, K = r.T, r.K
+        w = to_dev(r.weights.reshape(-1), DEV)
+        y = p.moe_padded_scatter(xp, route.indices, route.bin_ids, route.bins, route.padded_bins, w, T, K,
+                                 positions=route.positions, status=st)
+        o_y = oracle.padded_scatter(o_xp, o["indices"], o["bin_ids"], o["bins"], o["padded_bins"], r.weights, T, K)
+        check_scatter(to_host(y), o_y, r.name + " fused padded_scatter (oversized expert tensor)")
+        wg = p.moe_padded_wgrad(xp, to_dev(r.grad, DEV), route.indices, route.bin_ids, route.bins, route.padded_bins,
+                                K, positions=route.positions, status=st)
+        o_wg = oracle.padded_wgrad(o_xp, r.grad, o["indices"], o["bin_ids"], o["bins"], o["padded_bins"], K)
+        assert_close_fp32(to_host(wg), o_wg, r.name + " fused padded_wgrad (oversized expert tensor)")
     torch.cuda.synchronize()
     assert int(st.item()) == 0, "device status %d on valid input" % int(st.item())
 

@@ -205,8 +205,11 @@ __device__ void block_scan_experts(int64_t* v, int64_t* pv, int32_t E, int32_t m
 // per-chunk counts of the hist pass and every CTA derives what the scan pass
 // would have given it — its column prefix over the chunks before it and the
 // exclusive scan over experts of the totals — from the whole count matrix
-// (read from L2); CTA 0 also writes bins and padded_bins. One launch fewer,
-// and still no CTA waits on another.
+// (read from L2, with every thread of the CTA summing a share of the chunks
+// of one expert); CTA 0 also writes bins and padded_bins. One launch fewer,
+// and still no CTA waits on another. The chunk's expert ids are loaded
+// first, so their latency overlaps the count reads (route build at the
+// DeepSeek-V3 batch 14.7 -> 14.0 us with both).
 template <bool FUSED>
 __global__ void route_scatter_kernel(const int32_t* __restrict__ top_expert, int64_t n, int32_t E,
                                      const int32_t* __restrict__ offsets, int64_t G, int32_t m,
@@ -218,18 +221,52 @@ __global__ void route_scatter_kernel(const int32_t* __restrict__ top_expert, int
   __shared__ int64_t warp_sum[kMaxWarps][2];
   const int warps = blockDim.x / kWarp;
   const int warp = threadIdx.x / kWarp, lane = lane_id();
-  for (int q = threadIdx.x; q < warps * E; q += blockDim.x) whist[q] = 0;
+  // This chunk's expert ids first: their loads overlap the count reads below.
+  const int64_t base = (int64_t)blockIdx.x * blockDim.x * kRounds + (int64_t)warp * kWarp * kRounds;
+  int32_t ex[kRounds];
+#pragma unroll
+  for (int r = 0; r < kRounds; ++r) ex[r] = load_expert(top_expert, base + r * kWarp + lane, n, E, nullptr);
   int64_t* spre = reinterpret_cast<int64_t*>(whist + ((warps * E + 1) & ~1));  // prefix over earlier chunks
   int64_t* stot = spre + E;                                                     // total per expert
   int64_t* sst = stot + E;                                                      // exclusive start per expert
   int64_t* spst = sst + E;                                                      // padded start (CTA 0)
   if (FUSED) {
-    for (int e = threadIdx.x; e < E; e += blockDim.x) {
-      int64_t pre = 0, tot = 0;
-      for (int64_t g = 0; g < G; ++g) {
+    // Column sums over the chunks, split over `parts` threads per expert
+    // (their partial sums parked in whist before it is cleared), loads
+    // issued eight at a time.
+    int parts = (int)(blockDim.x / E);
+    if (parts > warps / 2) parts = warps / 2;
+    if (parts < 1) parts = 1;
+    const int64_t per = (G + parts - 1) / parts;
+    for (int t = threadIdx.x; t < E * parts; t += blockDim.x) {
+      const int e = t % E, part = t / E;
+      const int64_t g0 = part * per, g1 = min(G, g0 + per);
+      int32_t pre = 0, tot = 0;
+      int64_t g = g0;
+      for (; g + 8 <= g1; g += 8) {
+        int32_t c[8];
+#pragma unroll
+        for (int q = 0; q < 8; ++q) c[q] = __ldg(offsets + (g + q) * E + e);
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+          pre += (g + q) < (int64_t)blockIdx.x ? c[q] : 0;
+          tot += c[q];
+        }
+      }
+      for (; g < g1; ++g) {
         const int32_t c = __ldg(offsets + g * E + e);
         pre += g < (int64_t)blockIdx.x ? c : 0;
         tot += c;
+      }
+      whist[(2 * part) * E + e] = pre;
+      whist[(2 * part + 1) * E + e] = tot;
+    }
+    __syncthreads();
+    for (int e = threadIdx.x; e < E; e += blockDim.x) {
+      int64_t pre = 0, tot = 0;
+      for (int part = 0; part < parts; ++part) {
+        pre += whist[(2 * part) * E + e];
+        tot += whist[(2 * part + 1) * E + e];
       }
       spre[e] = pre;
       stot[e] = tot;
@@ -245,12 +282,11 @@ __global__ void route_scatter_kernel(const int32_t* __restrict__ top_expert, int
     }
   }
   __syncthreads();
-  const int64_t base = (int64_t)blockIdx.x * blockDim.x * kRounds + (int64_t)warp * kWarp * kRounds;
+  for (int q = threadIdx.x; q < warps * E; q += blockDim.x) whist[q] = 0;
+  __syncthreads();
   int32_t* mine = whist + warp * E;
-  int32_t ex[kRounds];
 #pragma unroll
   for (int r = 0; r < kRounds; ++r) {
-    ex[r] = load_expert(top_expert, base + r * kWarp + lane, n, E, nullptr);
     const unsigned peers = __match_any_sync(0xffffffffu, ex[r]);
     if (ex[r] >= 0 && lane == __ffs(peers) - 1) mine[ex[r]] += __popc(peers);
     __syncwarp();

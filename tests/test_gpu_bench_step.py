@@ -1,6 +1,6 @@
 """The benchmark's step runs the binned and padded branches on two streams
-(they depend only on the route build) and joins them before the compaction
-backward. This checks that the concurrent step computes exactly what the
+(they depend only on the route build) and the compaction backward on a
+third as soon as the padded wgrad it reads is done. This checks that the concurrent step computes exactly what the
 same ops compute one after another on one stream: every output of both
 branches and the dense router gradient, bit for bit (every kernel on the
 path is deterministic), on the first 1024 tokens of the DeepSeek-V3-shaped
@@ -34,12 +34,12 @@ def test_two_stream_step_matches_one_stream_ops():
         f()
     torch.cuda.synchronize(dev)
     want = {k: getattr(path, k).clone() for k in OUTPUTS}
-    side = torch.cuda.Stream(dev)
+    side, tail = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
     for _ in range(3):
         for k in OUTPUTS:
             getattr(path, k).fill_(float("nan") if getattr(path, k).is_floating_point() else 0)
         torch.cuda.synchronize(dev)
-        path.step(side)
+        path.step(side, tail)
         torch.cuda.synchronize(dev)
         for k in OUTPUTS:
             got = getattr(path, k)

@@ -469,6 +469,18 @@ def run_gpu(args, rank, world, local_rank):
         t_host = time.perf_counter() - t_host
     step_ms = [a.elapsed_time(b) for a, b in ev_step]
     total_ms = max_over_ranks(float(sum(step_ms)), dist, dev)
+    # For comparison, the same steps with every op on one stream, one after
+    # another (no events between the ops).
+    ev_seq = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(args.steps)]
+    for s in range(args.steps):
+        l2_flush(flush)
+        ev_seq[s][0].record(stream)
+        for _, _, f in ops:
+            f()
+        ev_seq[s][1].record(stream)
+    barrier()
+    one_stream_ms = max_over_ranks(float(sum(a.elapsed_time(b) for a, b in ev_seq)), dist, dev) / args.steps
     # Per-kernel breakdown: the ops again, one after another on one stream,
     # with an event after every op.
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(len(ops) + 1)] for _ in range(args.steps)]
@@ -522,6 +534,7 @@ def run_gpu(args, rank, world, local_rank):
         "config": workload_config(r),
         "hbm_gbs_gather_scatter_wgrad": round(hot_bytes / (hot_ms * 1e-3) / 1e9, 1),
         "step_gbs": round(sum(algo.values()) / (ms_per_step * 1e-3) / 1e9, 1),
+        "ms_per_step_one_stream": round(one_stream_ms, 5),
         "step_frac_of_%s_peak" % peak_kind: round(sum(algo.values()) / (ms_per_step * 1e-3) / 1e9 / peak, 4),
         "kernels_ms_sum": round(sum(v["ms"] for v in kern.values()), 5),
         "kernels": kern,

@@ -66,7 +66,8 @@ enum moe_dtype { MOE_F32 = 0, MOE_BF16 = 1 };
 /* Bits OR-ed into *d_status by kernels that meet invalid device data. */
 enum moe_device_status {
   MOE_STATUS_BAD_EXPERT = 1,   /* expert id outside [0, E) */
-  MOE_STATUS_BAD_INDEX = 2,    /* an index or position outside its range */
+  MOE_STATUS_BAD_INDEX = 2,    /* an index or position outside its range, or a positions
+                                   entry that indices does not map back (indices[positions[a]] != a) */
   MOE_STATUS_BAD_BINS = 4,     /* bins / padded_bins not monotonic or not consistent */
   MOE_STATUS_ROWS_MISMATCH = 8, /* padded_bins[E-1] exceeds the rows the caller provided */
   MOE_STATUS_TIMEOUT = 16       /* a bounded wait on an asynchronous copy gave up: the launch's
@@ -254,9 +255,10 @@ int moe_padded_gather_weighted(const void* dy, int32_t dtype,
  * [binned] Workflow steps 1-3): exactly moe_route_build of
  * top_expert [n = T*top_k] (all five outputs, positions required) followed
  * by moe_binned_gather / moe_padded_gather of x given those positions, with
- * the same results: four launches (the route build's three and the
- * gather's token pass), x read once per token. Its value over the two calls
- * is that the caller needs no positions buffer of its own between them.
+ * the same results: three or four launches (the route build's two, or
+ * three when its count matrix is large, and the gather's token pass), x
+ * read once per token. It is the two calls in one; a single launch is not
+ * offered (every output row depends on the counts of every chunk).
  *   workspace: >= moe_route_build_workspace_size(n, E) bytes.
  *   padded: out has out_rows rows; the caller does not know
  *   padded_bins[E-1] before the call, so out_rows is a bound, such as

@@ -868,7 +868,8 @@ def run_profile_case(args):
     `--profile-ops` once more, in that order, so that an ncu capture with
     `-k <kernel> -s <launches of that kernel in the warm-up pass>` sees
     exactly the second pass. Besides the step's ops (and the next rows'
-    `topk_gating`), `qwen_compaction_fwd` / `qwen_compaction_bwd` run the
+    `topk_gating`, and `binned_gather_weighted` / `padded_gather_weighted`
+    when one of them is named), `qwen_compaction_fwd` / `qwen_compaction_bwd` run the
     compaction on its own Qwen2-MoE-57B-shaped map (T=65536, E=64, topk=8),
     once as warm-up and once more when named."""
     import torch
@@ -886,6 +887,14 @@ def run_profile_case(args):
     qpi = torch.empty((q.probs.shape[0], q.topk), dtype=torch.float32, device=dev)
     qidx = torch.empty((q.probs.shape[0], q.topk), dtype=torch.int32, device=dev)
     qgp = torch.empty_like(qp)
+    if any(name.endswith("_gather_weighted") for name in args.profile_ops.split(",")):
+        gwb, gwp = torch.empty_like(path.xb), torch.empty_like(path.xp)
+        rt, w = path.route, path.pi.view(-1)
+        ops["binned_gather_weighted"] = lambda: path.p.moe_binned_gather_weighted(
+            path.grad, rt.indices, rt.bins, w, r.E, r.capacity, r.K, out=gwb, positions=rt.positions)
+        ops["padded_gather_weighted"] = lambda: path.p.moe_padded_gather_weighted(
+            path.grad, rt.indices, rt.bins, rt.padded_bins, w, r.K, out_rows=path.P, out=gwp,
+            positions=rt.positions)
     ops["qwen_compaction_fwd"] = lambda: path.p.moe_routing_map_to_indices_fwd(qp, qm, q.topk, out=(qpi, qidx))
     ops["qwen_compaction_bwd"] = lambda: path.p.moe_routing_map_to_indices_bwd(qg, qidx, q.probs.shape[1], out=qgp)
     for name in ops:

@@ -515,14 +515,16 @@ def test_corrupt_bins_and_positions_are_reported():
     assert int(st.item()) & _lib.MOE_STATUS_ROWS_MISMATCH
 
 
-@pytest.mark.parametrize("dtype", [wl.F32, wl.BF16])
-def test_scatter_flags_swapped_positions(dtype):
+@pytest.mark.parametrize("dtype,H,K", [(wl.F32, 40, 3), (wl.BF16, 40, 3), (wl.BF16, 40, 12), (wl.F32, 7, 3),
+                                       (wl.BF16, 7, 12)])
+def test_scatter_flags_swapped_positions(dtype, H, K):
     """A valid route's positions with two entries exchanged (every entry in
     range, the vector still a permutation) sets MOE_STATUS_BAD_INDEX in both
     scatters, and neither misrouted slot reaches the output: each token equals
     the oracle's combine with those two slots left out (weight 0, which adds a
-    signed zero and so leaves the fp32 sum unchanged)."""
-    r = wl.uniform_routing("swapped", 48, 40, 6, 3, dtype, capacity=20, pad_multiple=4, seed=31)
+    signed zero and so leaves the fp32 sum unchanged). TOP_K 12 and rows of 7
+    elements take the register scatter; the others the cp.async one."""
+    r = wl.uniform_routing("swapped", 48, H, 16, K, dtype, capacity=60, pad_multiple=4, seed=31)
     T, H, E, K = r.T, r.H, r.E, r.K
     n = T * K
     o = oracle.route_build(r.top_expert, E, r.pad_multiple)

@@ -9,7 +9,8 @@ multiple 128, bf16 activations, Zipf(1.1) expert popularity):
   of the padded wgrad on a third stream as soon as that wgrad is done.
 The two branches depend only on the route build, so they run concurrently;
 the per-kernel breakdown (`kernels`) times the same ops one after another
-on one stream.
+on one stream, and `kernels_alone` times each op by itself (5 warm-up
+launches, then the median of 20, each after an L2 flush).
 The expert FFN between gather and scatter is the identity (it is not part of
 the routing path), so scatter combines the gathered rows themselves.
 
@@ -496,6 +497,11 @@ def run_gpu(args, rank, world, local_rank):
         for q, (name, _, _) in enumerate(ops):
             per_kernel[name].append(ev[s][q].elapsed_time(ev[s][q + 1]))
 
+    # Each op alone, as the measurement plan times the gather / scatter /
+    # wgrad bandwidth bar: 5 warm-up launches, then 20 launches each after an
+    # L2 flush (not timed), the median.
+    alone = {name: time_op_median(f, flush, stream) for name, _, f in ops}
+
     e2e = run_e2e(args, path, dev, dist)
     next_rows = time_next_rows(args, path, flush, stream)
 
@@ -520,6 +526,14 @@ def run_gpu(args, rank, world, local_rank):
         if name in no_reuse:
             kern[name]["no_reuse_bytes"] = no_reuse[name]
             kern[name]["no_reuse_gbs"] = round(no_reuse[name] / (ms * 1e-3) / 1e9, 1)
+    kern_alone = {}
+    for name, ms_list in alone.items():
+        med = statistics.median(ms_list)
+        gbs = algo[name] / (med * 1e-3) / 1e9
+        kern_alone[name] = {"ms_median": round(med, 5), "ms_min": round(min(ms_list), 5),
+                            "ms_max": round(max(ms_list), 5), "gbs": round(gbs, 1),
+                            "frac_of_%s_peak" % peak_kind: round(gbs / peak, 4),
+                            "frac_of_nominal_8tbs": round(gbs / NOMINAL_HBM_GBS, 4)}
     hot = ["binned_gather", "binned_scatter", "binned_wgrad", "padded_gather", "padded_scatter", "padded_wgrad"]
     hot_bytes = sum(algo[k] for k in hot)
     hot_ms = sum(kern[k]["ms"] for k in hot)
@@ -538,6 +552,7 @@ def run_gpu(args, rank, world, local_rank):
         "step_frac_of_%s_peak" % peak_kind: round(sum(algo.values()) / (ms_per_step * 1e-3) / 1e9 / peak, 4),
         "kernels_ms_sum": round(sum(v["ms"] for v in kern.values()), 5),
         "kernels": kern,
+        "kernels_alone": kern_alone,
         "roofline": {"bound": "hbm", "kernel": dominant, "achieved": ach, "peak": peak, "peak_kind": peak_kind,
                      "unit": "GB/s", "frac": round(ach / peak, 4),
                      "traffic": traffic_from_profiles(dominant, libbuild.kernel_digest(KERNEL_UNIT[dominant]))},
@@ -591,6 +606,27 @@ def time_compaction_workload(args, path, flush, stream) -> dict:
                           T * E + T * k * 4 + T * k * 8, flush, stream),
         "bwd": time_alone(args, lambda: p.moe_routing_map_to_indices_bwd(gpi, idx, E, out=gp),
                           T * k * 8 + T * E * 4, flush, stream)}}
+
+
+def time_op_median(fn, flush, stream, warmup=5, reps=20) -> list:
+    """CUDA-event times (ms) of `fn` on `stream`: `warmup` untimed launches,
+    then `reps` timed ones, each after an L2 flush that is not timed."""
+    import torch
+
+    for _ in range(warmup):
+        l2_flush(flush)
+        fn()
+    ev = []
+    for _ in range(reps):
+        l2_flush(flush)
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        fn()
+        b.record(stream)
+        ev.append((a, b))
+    torch.cuda.synchronize()
+    return [a.elapsed_time(b) for a, b in ev]
 
 
 def time_alone(args, fn, nbytes, flush, stream) -> dict:

@@ -306,6 +306,7 @@ class Path:
             self.g_out = (self.torch.empty((T, K), dtype=self.torch.int32, device=self.dev),
                           self.torch.empty((T, K), dtype=self.torch.float32, device=self.dev))
             self.froute = p.Route(*(self.torch.empty_like(t) for t in rt))
+            self.ws_one = p.ops.route_workspace(self.n, E, self.dev, with_gather=True)
         algo = self.algorithmic_bytes()
         return [
             ("topk_gating", lambda: p.moe_topk_gating(self.logits, K, "sigmoid", True, out=self.g_out),
@@ -325,6 +326,14 @@ class Path:
             ("route_build_padded_gather",
              lambda: p.moe_route_build_padded_gather(self.idx, self.x, E, r.pad_multiple, out_rows=self.P,
                                                      route=self.froute, out=self.gwp, workspace=self.ws),
+             algo["route_build"] + algo["padded_gather"]),
+            ("route_build_binned_gather_one_launch",
+             lambda: p.moe_route_build_binned_gather(self.idx, self.x, E, r.capacity, r.pad_multiple,
+                                                     route=self.froute, out=self.gwb, workspace=self.ws_one),
+             algo["route_build"] + algo["binned_gather"]),
+            ("route_build_padded_gather_one_launch",
+             lambda: p.moe_route_build_padded_gather(self.idx, self.x, E, r.pad_multiple, out_rows=self.P,
+                                                     route=self.froute, out=self.gwp, workspace=self.ws_one),
              algo["route_build"] + algo["padded_gather"]),
         ]
 

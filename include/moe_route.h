@@ -255,19 +255,40 @@ int moe_padded_gather_weighted(const void* dy, int32_t dtype,
  * [binned] Workflow steps 1-3): exactly moe_route_build of
  * top_expert [n = T*top_k] (all five outputs, positions required) followed
  * by moe_binned_gather / moe_padded_gather of x given those positions, with
- * the same results: three or four launches (the route build's two, or
- * three when its count matrix is large, and the gather's token pass), x
- * read once per token. It is the two calls in one; a single launch is not
- * offered (every output row depends on the counts of every chunk).
- *   workspace: >= moe_route_build_workspace_size(n, E) bytes.
+ * the same results, x read once per token.
+ *   One launch when the bulk-copy gather applies (rows a multiple of 16
+ *   bytes, x and out 16-byte aligned), E <= 1024, the workspace is 8-byte
+ *   aligned and holds moe_route_build_gather_workspace_size(n, E) bytes,
+ *   and the device accepts a cooperative launch (all CTAs resident): the
+ *   CTAs count, scan and scatter the routing data between grid-wide
+ *   barriers and then copy the rows. Each barrier wait is bounded; a CTA
+ *   that gives up sets MOE_STATUS_TIMEOUT and stops (outputs then
+ *   unspecified). The barrier word in the workspace needs no
+ *   initialisation, but two such calls must not use one workspace at the
+ *   same time. Otherwise three or four launches (the route build's two or
+ *   three and the gather's token pass, chained by programmatic dependent
+ *   launch), needing only moe_route_build_workspace_size(n, E) bytes of
+ *   workspace. On GB300 the chained launches measured faster at every batch
+ *   size tried (16 to 8192 tokens of the DeepSeek-V3 shape: the single
+ *   launch's three grid barriers cost more than the launches they replace),
+ *   so the larger workspace is for callers that want exactly one kernel.
  *   padded: out has out_rows rows; the caller does not know
  *   padded_bins[E-1] before the call, so out_rows is a bound, such as
  *   n + E*(pad_multiple-1) (every padded total is at most that); rows at
  *   or beyond padded_bins[E-1] are zero-filled, and MOE_STATUS_ROWS_MISMATCH
  *   is set if padded_bins[E-1] exceeds out_rows.
  * Errors as for the two calls; argument errors return before anything is
- * enqueued.
+ * enqueued. An expert id outside [0, E) sets MOE_STATUS_BAD_EXPERT (its
+ * position entry is -1 on the one-launch path; outputs unspecified).
  */
+size_t moe_route_build_gather_workspace_size(int64_t n, int32_t num_experts);
+/*
+ * Testing only: raises the target of every grid barrier of the one-launch
+ * route build + gather by `extra` arrivals (0 restores it), so that the
+ * bounded waits run out and the call reports MOE_STATUS_TIMEOUT without any
+ * fault. Process-wide; not for concurrent use with real calls.
+ */
+void moe_test_barrier_slack(uint32_t extra);
 int moe_route_build_binned_gather(const int32_t* top_expert, const void* x,
                                   int32_t dtype, int64_t num_tokens,
                                   int64_t hidden, int32_t num_experts,

@@ -32,6 +32,8 @@ SIGNATURES = {
     "moe_error_string": (ctypes.c_char_p, [ctypes.c_int]),
     "moe_version": (ctypes.c_int, []),
     "moe_route_build_workspace_size": (_SZ, [_I64, _I32]),
+    "moe_route_build_gather_workspace_size": (_SZ, [_I64, _I32]),
+    "moe_test_barrier_slack": (None, [ctypes.c_uint32]),
     "moe_route_build": (ctypes.c_int, [_P, _I64, _I32, _I32, _P, _P, _P, _P, _P, _P, _SZ, _P, _P]),
     "moe_route_build_noalloc": (ctypes.c_int, [_P, _I64, _I32, _I32, _P, _P, _P, _P, _P, _P, _P]),
     "moe_check_routing": (ctypes.c_int, [_P, _P, _P, _P, _P, _I64, _I32, _P, _P]),

@@ -417,13 +417,22 @@ constexpr size_t kTmaSmem = (size_t)kTmaChunk * (1 + 2 * kTmaWarps) + 16 * kTmaW
 #define MOE_GATHER_ITEMS 0
 #endif
 
-template <bool PADDED>
-__global__ void __launch_bounds__(tma_threads<PADDED>(), 1) gather_tma_kernel(GatherArgs g, int64_t row_bytes) {
-  await_previous_kernel();
+// Routing data the token pass reads: FRESH = written earlier in the same
+// launch by other CTAs (coherent loads through L2), else unchanged for the
+// whole launch (read-only path).
+template <bool FRESH>
+__device__ __forceinline__ int32_t ld_route(const int32_t* p) {
+  if constexpr (FRESH) return __ldcg(p);
+  else return __ldg(p);
+}
+
+// The bulk-copy pass itself, after the caller has staged bins (and padded
+// bins) in sb / spb (or points them at global memory): every thread of the
+// CTA calls it. `tsm` is the kTmaSmem bytes of dynamic shared memory.
+template <bool PADDED, bool FRESH>
+__device__ __forceinline__ void tma_copy_pass(const GatherArgs& g, int64_t row_bytes, const int32_t* sb,
+                                              const int32_t* spb, unsigned char* tsm) {
   constexpr unsigned kAll = 0xffffffffu;
-  extern __shared__ __align__(128) unsigned char tsm[];
-  __shared__ int32_t sbins[kStageMax];
-  __shared__ int32_t spbins[PADDED ? kStageMax : 1];
   const int warp = threadIdx.x / kWarp, lane = lane_id();
   unsigned char* zero = tsm;
   constexpr int kZeroWarps = zero_warps<PADDED>();
@@ -435,24 +444,17 @@ __global__ void __launch_bounds__(tma_threads<PADDED>(), 1) gather_tma_kernel(Ga
     mbar_init(smem_u32(bars));
     mbar_init(smem_u32(bars + 1));
   }
-  const bool staged = g.E <= kStageMax;
-  if (staged) {
-    for (int e = threadIdx.x; e < g.E; e += blockDim.x) {
-      sbins[e] = __ldg(g.bins + e);
-      if (PADDED) spbins[e] = __ldg(g.padded_bins + e);
-    }
-  }
   fence_mbarrier_init();
   fence_async_shared();  // the zero chunk and the barriers, for the bulk-copy unit
   __syncthreads();
-  const int32_t* sb = staged ? sbins : g.bins;
-  const int32_t* spb = PADDED ? (staged ? spbins : g.padded_bins) : nullptr;
   if (blockIdx.x == 0) {
-    for (int e = threadIdx.x; e < g.E; e += blockDim.x) {
-      const int32_t prev = e > 0 ? sb[e - 1] : 0;
-      bool ok = sb[e] >= prev && (e < g.E - 1 || sb[e] <= g.n);
-      if (PADDED) ok = ok && (int64_t)spb[e] - (e > 0 ? spb[e - 1] : 0) >= (int64_t)sb[e] - prev;
-      if (!ok) flag_status(g.status, MOE_STATUS_BAD_BINS);
+    if (!FRESH) {  // bins computed in the same launch need no check
+      for (int e = threadIdx.x; e < g.E; e += blockDim.x) {
+        const int32_t prev = e > 0 ? sb[e - 1] : 0;
+        bool ok = sb[e] >= prev && (e < g.E - 1 || sb[e] <= g.n);
+        if (PADDED) ok = ok && (int64_t)spb[e] - (e > 0 ? spb[e - 1] : 0) >= (int64_t)sb[e] - prev;
+        if (!ok) flag_status(g.status, MOE_STATUS_BAD_BINS);
+      }
     }
     if (PADDED && threadIdx.x == 0 && spb[g.E - 1] > g.rows_out) flag_status(g.status, MOE_STATUS_ROWS_MISMATCH);
   }
@@ -495,8 +497,8 @@ __global__ void __launch_bounds__(tma_threads<PADDED>(), 1) gather_tma_kernel(Ga
       const int64_t a = t * g.top_k + k0 + lane;
       int64_t row = -1;
       if (k0 + lane < g.top_k) {
-        const int32_t i = __ldg(g.positions + a);
-        if (i < 0 || i >= g.n || __ldg(g.indices + i) != a) {
+        const int32_t i = ld_route<FRESH>(g.positions + a);
+        if (i < 0 || i >= g.n || ld_route<FRESH>(g.indices + i) != a) {
           flag_status(g.status, MOE_STATUS_BAD_INDEX);
         } else {
           row = position_row<PADDED>(g, sb, spb, i);
@@ -540,26 +542,368 @@ __global__ void __launch_bounds__(tma_threads<PADDED>(), 1) gather_tma_kernel(Ga
   }
 }
 
+template <bool PADDED>
+__global__ void __launch_bounds__(tma_threads<PADDED>(), 1) gather_tma_kernel(GatherArgs g, int64_t row_bytes) {
+  await_previous_kernel();
+  extern __shared__ __align__(128) unsigned char tsm[];
+  __shared__ int32_t sbins[kStageMax];
+  __shared__ int32_t spbins[PADDED ? kStageMax : 1];
+  const bool staged = g.E <= kStageMax;
+  if (staged) {
+    for (int e = threadIdx.x; e < g.E; e += blockDim.x) {
+      sbins[e] = __ldg(g.bins + e);
+      if (PADDED) spbins[e] = __ldg(g.padded_bins + e);
+    }
+  }
+  tma_copy_pass<PADDED, false>(g, row_bytes, staged ? sbins : g.bins,
+                               PADDED ? (staged ? spbins : g.padded_bins) : nullptr, tsm);
+}
+
+// ------------------------------------- route build + bulk-copy gather, one launch
+//
+// One cooperative launch (every CTA resident at once) runs the route build
+// and the gather's token pass, the phases separated by grid barriers:
+//   A  CTA c counts the expert ids of its chunk of assignments (contiguous,
+//      one sub-range per warp, per-warp counts kept in shared memory) and
+//      writes them as row c of the count matrix;
+//   B1 one warp per expert turns its column into an exclusive prefix over
+//      the chunks and writes the expert's total;
+//   B2 every CTA scans the totals over experts into bins and padded_bins
+//      (CTA 0 writes them out; every CTA keeps them staged for C) and gives
+//      each assignment of its chunk its stable sorted position (expert start
+//      + the chunk prefix + the warp prefix + the rank among equal ids in a
+//      warp round), writing indices, bin_ids and positions;
+//   C  the bulk-copy token pass, reading those positions (coherent loads).
+// The barrier counts CTA arrivals in one 64-bit word of the workspace whose
+// upper 48 bits carry a per-call tag, so the word needs no initialisation
+// (a stale value from an earlier call is re-tagged by the first arrival);
+// each wait is bounded and a CTA that gives up sets MOE_STATUS_TIMEOUT and
+// leaves, so every CTA ends.
+
+struct RouteGatherArgs {
+  const int32_t* top_expert;
+  int32_t* indices;
+  int32_t* bin_ids;
+  int32_t* bins;
+  int32_t* padded_bins;
+  int32_t* positions;
+  int32_t* counts;              // [grid][E] count matrix, then [E] totals
+  unsigned long long* barrier;  // the barrier word
+  unsigned long long tag;       // this call's tag (low 16 bits zero)
+  int32_t m;                    // padding multiple
+  int64_t chunk;                // assignments per CTA
+  uint32_t slack = 0;           // added to every barrier's target (testing: makes the waits run out)
+};
+
+constexpr unsigned long long kTagMask = ~0xffffull;
+
+__device__ __forceinline__ unsigned long long ld_acquire_u64(const unsigned long long* p) {
+  unsigned long long v;
+  asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+  return v;
+}
+
+// Arrive at the grid barrier and wait until `target` CTAs of this call have
+// arrived (bounded). Every thread of the CTA calls it; all get the result.
+__device__ bool grid_barrier(const RouteGatherArgs& f, uint32_t target, int32_t* status) {
+  __shared__ int passed;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    __threadfence();  // this CTA's writes before its arrival
+    bool arrived = false;
+    for (int it = 0; it < 4096 && !arrived; ++it) {
+      const unsigned long long cur = ld_acquire_u64(f.barrier);
+      if ((cur & kTagMask) == f.tag) {
+        atomicAdd(f.barrier, 1ull);
+        arrived = true;
+      } else if (atomicCAS(f.barrier, cur, f.tag | 1ull) == cur) {
+        arrived = true;  // first arrival of this call: the word is re-tagged
+      }
+    }
+    bool ok = false;
+    for (int it = 0; arrived && it < kSpinLimit; ++it) {
+      const unsigned long long cur = ld_acquire_u64(f.barrier);
+      if ((cur & kTagMask) == f.tag && (uint32_t)(cur & 0xffffull) >= target) {
+        ok = true;
+        break;
+      }
+      __nanosleep(64);
+    }
+    if (!ok) flag_status(status, MOE_STATUS_TIMEOUT);
+    __threadfence();
+    passed = ok;
+  }
+  __syncthreads();
+  return passed != 0;
+}
+
+// Exclusive scan over experts of v[e] (in place) and of its rounding up to
+// multiples of m (into pv); every thread of the CTA calls it.
+__device__ void scan_experts(int64_t* v, int64_t* pv, int32_t E, int32_t m, int64_t (*wsum)[2]) {
+  const int nt = blockDim.x, lane = lane_id(), warp = threadIdx.x / kWarp;
+  const int per = (E + nt - 1) / nt;
+  const int lo = min((int)threadIdx.x * per, (int)E), hi = min(lo + per, (int)E);
+  int64_t s = 0, ps = 0;
+  for (int e = lo; e < hi; ++e) {
+    s += v[e];
+    ps += (v[e] + m - 1) / m * m;
+  }
+  int64_t xs = s, xps = ps;  // inclusive over the warp's threads
+#pragma unroll
+  for (int d = 1; d < kWarp; d <<= 1) {
+    const int64_t a = __shfl_up_sync(0xffffffffu, xs, d);
+    const int64_t b = __shfl_up_sync(0xffffffffu, xps, d);
+    if (lane >= d) {
+      xs += a;
+      xps += b;
+    }
+  }
+  if (lane == kWarp - 1) {
+    wsum[warp][0] = xs;
+    wsum[warp][1] = xps;
+  }
+  __syncthreads();
+  int64_t run = xs - s, prun = xps - ps;
+  for (int w = 0; w < warp; ++w) {
+    run += wsum[w][0];
+    prun += wsum[w][1];
+  }
+  for (int e = lo; e < hi; ++e) {
+    const int64_t c = v[e];
+    v[e] = run;
+    pv[e] = prun;
+    run += c;
+    prun += (c + m - 1) / m * m;
+  }
+  __syncthreads();
+}
+
+template <bool PADDED>
+__global__ void __launch_bounds__(tma_threads<PADDED>(), 1)
+    route_gather_kernel(GatherArgs g, int64_t row_bytes, RouteGatherArgs f) {
+  constexpr unsigned kAll = 0xffffffffu;
+  constexpr int kWarpsCta = tma_threads<PADDED>() / kWarp;
+  extern __shared__ __align__(128) unsigned char tsm[];
+  __shared__ int32_t sbins[kStageMax];
+  __shared__ int32_t spbins[PADDED ? kStageMax : 1];
+  __shared__ int64_t wsum[kWarpsCta][2];
+  const int E = g.E;
+  const int warp = threadIdx.x / kWarp, lane = lane_id();
+  const int64_t G = gridDim.x;
+  // Phases A and B use the bulk-copy buffers' shared memory:
+  int32_t* whist = reinterpret_cast<int32_t*>(tsm);  // [warps][E]: counts, then running offsets
+  int64_t* sstart = reinterpret_cast<int64_t*>(tsm + ((size_t)kWarpsCta * E * 4 + 7) / 8 * 8);  // [E]
+  int64_t* spstart = sstart + E;                                                            // [E]
+  int32_t* stotal = reinterpret_cast<int32_t*>(spstart + E);                                // [E]
+  int32_t* spre = stotal + E;                                                               // [E]
+  int32_t* totals = f.counts + G * E;
+
+  // A: per-warp counts over contiguous sub-ranges of the chunk.
+  const int64_t c0 = min((int64_t)blockIdx.x * f.chunk, g.n), c1 = min(c0 + f.chunk, g.n);
+  const int64_t sub = (c1 - c0 + kWarpsCta - 1) / kWarpsCta;
+  const int64_t s0 = min(c0 + warp * sub, c1), s1 = min(s0 + sub, c1);
+  for (int q = threadIdx.x; q < kWarpsCta * E; q += blockDim.x) whist[q] = 0;
+  __syncthreads();
+  int32_t* mine = whist + warp * E;
+  for (int64_t b = s0; b < s1; b += kWarp) {
+    int32_t e = -1;
+    if (b + lane < s1) {
+      e = __ldg(f.top_expert + b + lane);
+      if (e < 0 || e >= E) {
+        flag_status(g.status, MOE_STATUS_BAD_EXPERT);
+        e = -1;
+      }
+    }
+    const unsigned peers = __match_any_sync(kAll, e);
+    if (e >= 0 && lane == __ffs(peers) - 1) mine[e] += __popc(peers);
+    __syncwarp();
+  }
+  __syncthreads();
+  for (int e = threadIdx.x; e < E; e += blockDim.x) {
+    int32_t c = 0;
+    for (int w = 0; w < kWarpsCta; ++w) c += whist[w * E + e];
+    f.counts[(int64_t)blockIdx.x * E + e] = c;
+  }
+  if (!grid_barrier(f, (uint32_t)G + f.slack, g.status)) return;
+
+  // B1: a warp per expert: exclusive prefix of its column over the chunks,
+  // kColPer chunks per lane loaded at once and held in registers.
+  constexpr int kColPer = 16;
+  for (int64_t e = (int64_t)blockIdx.x * kWarpsCta + warp; e < E; e += G * kWarpsCta) {
+    int32_t carry = 0;
+    for (int64_t q0 = 0; q0 < G; q0 += kWarp * kColPer) {
+      const int64_t qb = q0 + (int64_t)lane * kColPer;
+      int32_t v[kColPer];
+      int32_t s = 0;
+#pragma unroll
+      for (int j = 0; j < kColPer; ++j) {
+        v[j] = qb + j < G ? __ldcg(f.counts + (qb + j) * E + e) : 0;
+        s += v[j];
+      }
+      int32_t x = s;  // inclusive over lanes
+#pragma unroll
+      for (int d = 1; d < kWarp; d <<= 1) {
+        const int32_t y = __shfl_up_sync(kAll, x, d);
+        if (lane >= d) x += y;
+      }
+      int32_t run = carry + x - s;
+#pragma unroll
+      for (int j = 0; j < kColPer; ++j) {
+        if (qb + j < G) f.counts[(qb + j) * E + e] = run;
+        run += v[j];
+      }
+      carry += __shfl_sync(kAll, x, kWarp - 1);
+    }
+    if (lane == 0) totals[e] = carry;
+  }
+  if (!grid_barrier(f, (uint32_t)(2 * G) + f.slack, g.status)) return;
+
+  // B2: bins from the totals, then this chunk's sorted positions.
+  for (int e = threadIdx.x; e < E; e += blockDim.x) {
+    const int32_t t = __ldcg(totals + e);
+    stotal[e] = t;
+    sstart[e] = t;
+    spre[e] = __ldcg(f.counts + (int64_t)blockIdx.x * E + e);
+  }
+  __syncthreads();
+  scan_experts(sstart, spstart, E, f.m, wsum);
+  for (int e = threadIdx.x; e < E; e += blockDim.x) {
+    const int32_t b = (int32_t)(sstart[e] + stotal[e]);
+    const int32_t pb = (int32_t)(spstart[e] + ((int64_t)stotal[e] + f.m - 1) / f.m * f.m);
+    sbins[e] = b;
+    if (PADDED) spbins[e] = pb;
+    if (blockIdx.x == 0) {
+      f.bins[e] = b;
+      if (f.padded_bins != nullptr) f.padded_bins[e] = pb;
+    }
+    int32_t run = (int32_t)sstart[e] + spre[e];
+    for (int w = 0; w < kWarpsCta; ++w) {
+      const int32_t c = whist[w * E + e];
+      whist[w * E + e] = run;
+      run += c;
+    }
+  }
+  __syncthreads();
+  const unsigned lt = lanemask_lt();
+  for (int64_t b = s0; b < s1; b += kWarp) {
+    const int64_t a = b + lane;
+    int32_t e = -1;
+    if (a < s1) {
+      e = __ldg(f.top_expert + a);
+      if (e < 0 || e >= E) {
+        e = -1;
+        f.positions[a] = -1;  // left out of every output (already flagged)
+      }
+    }
+    const unsigned peers = __match_any_sync(kAll, e);
+    if (e >= 0) {
+      const int32_t dst = mine[e] + __popc(peers & lt);
+      f.indices[dst] = (int32_t)a;
+      f.bin_ids[dst] = e;
+      f.positions[a] = dst;
+    }
+    __syncwarp();
+    if (e >= 0 && lane == __ffs(peers) - 1) mine[e] += __popc(peers);
+    __syncwarp();
+  }
+  if (!grid_barrier(f, (uint32_t)(3 * G) + f.slack, g.status)) return;
+
+  // C: the token pass over the positions just written.
+  tma_copy_pass<PADDED, true>(g, row_bytes, sbins, PADDED ? spbins : nullptr, tsm);
+}
+
+// Sets the dynamic shared-memory opt-in of a bulk-copy kernel once per device
+// (concurrent callers may both set it, which is harmless); false on failure.
+template <typename Kernel>
+bool allow_tma_smem(Kernel k, std::atomic<int>* configured, int n_devices) {
+  int dev = 0;
+  (void)cudaGetDevice(&dev);
+  const bool cached = dev >= 0 && dev < n_devices;
+  if (cached && configured[dev].load(std::memory_order_relaxed) != 0) return true;
+  if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kTmaSmem) != cudaSuccess) {
+    (void)cudaGetLastError();
+    return false;
+  }
+  if (cached) configured[dev].store(1, std::memory_order_relaxed);
+  return true;
+}
+
+// CTAs of the one-launch route build + gather on this device (all resident
+// at once), 0 when it cannot run here.
+template <bool PADDED>
+int64_t route_gather_grid() {
+  constexpr int kMaxDevices = 64;
+  static std::atomic<int> configured[kMaxDevices];
+  auto k = route_gather_kernel<PADDED>;
+  if (!allow_tma_smem(k, configured, kMaxDevices)) return 0;
+  int per_sm = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k, tma_threads<PADDED>(), kTmaSmem) != cudaSuccess) {
+    (void)cudaGetLastError();
+    return 0;
+  }
+  const int64_t grid = (int64_t)per_sm * num_sms();
+  return grid * 3 <= 0xffff ? grid : 0;  // three barriers' arrivals fit the word's 16-bit count
+}
+
+// Workspace of the one-launch path: the [grid][E] count matrix and [E]
+// totals (int32), then the 8-byte barrier word.
+size_t route_gather_workspace(int64_t grid, int32_t E) {
+  return ((size_t)(grid * E + E) * sizeof(int32_t) + 7) / 8 * 8 + 8;
+}
+
+std::atomic<unsigned long long> g_route_gather_calls{0};
+std::atomic<uint32_t> g_barrier_slack{0};  // moe_test_barrier_slack
+
+// Launches route build + bulk-copy gather as one cooperative kernel; false
+// when it does not apply (rows or pointers off the bulk-copy rules, too many
+// experts to stage, too small a workspace, or the launch refused), and the
+// caller then takes the multi-launch path.
+template <bool PADDED>
+bool launch_route_gather(const GatherArgs& g, int64_t row_bytes, RouteGatherArgs f, void* workspace,
+                         size_t workspace_bytes, cudaStream_t s, int* rc) {
+  if (!MOE_GATHER_TMA || row_bytes % 16 != 0 || !aligned(g.x, 16) || !aligned(g.out, 16)) return false;
+  if (g.E > kStageMax || g.n < 1 || g.rows_out < 1 || !aligned(workspace, 8)) return false;
+  const int64_t grid = route_gather_grid<PADDED>();
+  if (grid < 1 || workspace_bytes < route_gather_workspace(grid, g.E)) return false;
+  f.counts = static_cast<int32_t*>(workspace);
+  f.barrier = reinterpret_cast<unsigned long long*>(static_cast<char*>(workspace) +
+                                                    route_gather_workspace(grid, g.E) - 8);
+  f.tag = ((g_route_gather_calls.fetch_add(1, std::memory_order_relaxed) + 1) & 0xffffffffffffull) << 16;
+  f.chunk = (g.n + grid - 1) / grid;
+  f.slack = g_barrier_slack.load(std::memory_order_relaxed);
+  GatherArgs gt = g;
+  gt.positions = f.positions;
+  gt.row_begin = gt.rows_out;
+  gt.segs = MOE_TMA_SEGS;
+  gt.seg_len = ((row_bytes + gt.segs - 1) / gt.segs + 15) / 16 * 16;  // bytes, 16-byte multiples
+  gt.segs = (row_bytes + gt.seg_len - 1) / gt.seg_len;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)grid);
+  cfg.blockDim = dim3(tma_threads<PADDED>());
+  cfg.dynamicSmemBytes = kTmaSmem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeCooperative;  // every CTA resident at once: the grid barriers end
+  attr[0].val.cooperative = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (cudaLaunchKernelEx(&cfg, route_gather_kernel<PADDED>, gt, row_bytes, f) != cudaSuccess) {
+    (void)cudaGetLastError();
+    return false;
+  }
+  *rc = MOE_OK;
+  return true;
+}
+
 // Launches the bulk-copy token pass; false when the rows or pointers do not
 // meet the 16-byte rule of the bulk copies (the register path runs instead).
 template <bool PADDED>
 bool launch_gather_tma(const GatherArgs& g, int64_t row_bytes, cudaStream_t s, int* rc) {
   if (!MOE_GATHER_TMA || row_bytes % 16 != 0 || !aligned(g.x, 16) || !aligned(g.out, 16)) return false;
   auto k = gather_tma_kernel<PADDED>;
-  // The dynamic shared-memory opt-in is per device; set it once per device
-  // (concurrent callers may both set it, which is harmless).
   constexpr int kMaxDevices = 64;
   static std::atomic<int> configured[kMaxDevices];
-  int dev = 0;
-  (void)cudaGetDevice(&dev);
-  const bool cached = dev >= 0 && dev < kMaxDevices;
-  if (!cached || configured[dev].load(std::memory_order_relaxed) == 0) {
-    if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kTmaSmem) != cudaSuccess) {
-      (void)cudaGetLastError();
-      return false;
-    }
-    if (cached) configured[dev].store(1, std::memory_order_relaxed);
-  }
+  if (!allow_tma_smem(k, configured, kMaxDevices)) return false;
   GatherArgs gt = g;
   gt.segs = MOE_TMA_SEGS;
   gt.seg_len = ((row_bytes + gt.segs - 1) / gt.segs + 15) / 16 * 16;  // bytes, 16-byte multiples
@@ -745,11 +1089,39 @@ static int route_then_gather(const int32_t* top_expert, int32_t E, int32_t pad_m
                              cudaStream_t s) {
   if (positions == nullptr || (padded && padded_bins == nullptr)) return MOE_ERR_INVALID_ARG;
   if (g.out == nullptr && g.rows_out > 0 && g.vecs > 0) return MOE_ERR_INVALID_ARG;
+  // One launch when every host check of the route build passes and the
+  // bulk-copy pass applies; otherwise the route build's launches and the
+  // token pass (which also report any invalid argument).
+  const void* rptrs[] = {top_expert, indices, bin_ids, bins, padded_bins, positions};
+  bool route_ok = g.n > 0 && pad_multiple >= 1 && g.n + (int64_t)E * (pad_multiple - 1) <= INT32_MAX &&
+                  top_expert != nullptr && indices != nullptr && bin_ids != nullptr && bins != nullptr &&
+                  workspace != nullptr && workspace_bytes >= moe_route_build_workspace_size(g.n, E) &&
+                  g.rows_out > 0 && g.vecs > 0 && (g.weights == nullptr);
+  for (const void* p : rptrs) route_ok = route_ok && (p == nullptr || aligned(p, 4));
+  if (route_ok) {
+    const int64_t row_bytes = g.vecs * dtype_bytes(dtype);  // g.vecs holds H here
+    RouteGatherArgs f{top_expert, indices, bin_ids, bins, padded_bins, positions, nullptr, nullptr, 0, pad_multiple, 0};
+    int rc = MOE_OK;
+    if (padded ? launch_route_gather<true>(g, row_bytes, f, workspace, workspace_bytes, s, &rc)
+               : launch_route_gather<false>(g, row_bytes, f, workspace, workspace_bytes, s, &rc))
+      return rc;
+  }
   const int rc = moe_route_build(top_expert, g.n, E, pad_multiple, indices, bin_ids, bins, padded_bins, positions,
                                  workspace, workspace_bytes, g.status, reinterpret_cast<moe_stream_t>(s));
   if (rc != MOE_OK || g.rows_out == 0 || g.vecs == 0) return rc;
   g.positions = positions;
   return padded ? dispatch_gather<true>(g, dtype, s) : dispatch_gather<false>(g, dtype, s);
+}
+
+extern "C" void moe_test_barrier_slack(uint32_t extra) { g_barrier_slack.store(extra, std::memory_order_relaxed); }
+
+extern "C" size_t moe_route_build_gather_workspace_size(int64_t n, int32_t num_experts) {
+  const size_t route = moe_route_build_workspace_size(n, num_experts);
+  if (route == 0 || num_experts > kStageMax) return route;
+  const int64_t grid = max(route_gather_grid<true>(), route_gather_grid<false>());
+  if (grid < 1) return route;
+  const size_t fused = (route_gather_workspace(grid, num_experts) + 255) / 256 * 256;
+  return fused > route ? fused : route;
 }
 
 extern "C" int moe_route_build_binned_gather(const int32_t* top_expert, const void* x, int32_t dtype, int64_t T,

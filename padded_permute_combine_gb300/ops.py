@@ -59,9 +59,16 @@ class Route(NamedTuple):
     positions: torch.Tensor    # [n] int32
 
 
-def route_workspace(n: int, num_experts: int, device) -> torch.Tensor:
-    size = _lib.load().moe_route_build_workspace_size(n, num_experts)
-    return torch.empty(max(1, (size + 3) // 4), dtype=torch.int32, device=device)
+def route_workspace(n: int, num_experts: int, device, with_gather: bool = False) -> torch.Tensor:
+    """Workspace of moe_route_build, or (with_gather) the larger one with
+    which the route build + gather calls run as a single launch."""
+    lib = _lib.load()
+    if with_gather:
+        with torch.cuda.device(device):  # sized for this device's SM count
+            size = lib.moe_route_build_gather_workspace_size(n, num_experts)
+    else:
+        size = lib.moe_route_build_workspace_size(n, num_experts)
+    return torch.empty(max(2, (size + 7) // 8 * 2), dtype=torch.int32, device=device)
 
 
 def moe_route_build(top_expert: torch.Tensor, num_experts: int, pad_multiple: int = 1,
@@ -210,10 +217,12 @@ def _new_route(n: int, num_experts: int, dev) -> Route:
 
 def moe_route_build_binned_gather(top_expert: torch.Tensor, x: torch.Tensor, num_experts: int, capacity: int,
                                   pad_multiple: int = 1, route: Route | None = None, out: torch.Tensor | None = None,
-                                  workspace: torch.Tensor | None = None,
-                                  status: torch.Tensor | None = None) -> tuple[Route, torch.Tensor]:
+                                  workspace: torch.Tensor | None = None, status: torch.Tensor | None = None,
+                                  one_launch: bool = False) -> tuple[Route, torch.Tensor]:
     """Route build of top_expert [T, K] and binned gather of x [T, H] in one
-    call: (route, [E, capacity, H])."""
+    call: (route, [E, capacity, H]). one_launch: size the workspace for the
+    single cooperative launch (slower than the default chained launches on
+    GB300; for callers that want exactly one kernel)."""
     te = _need(top_expert, torch.int32, "top_expert")
     _need(x, None, "x", te.device)
     dt = _act_dtype(x, "x")
@@ -227,7 +236,7 @@ def moe_route_build_binned_gather(top_expert: torch.Tensor, x: torch.Tensor, num
     if out is None:
         out = torch.empty((num_experts, capacity, H), dtype=x.dtype, device=x.device)
     _need(out, x.dtype, "out", x.device)
-    ws = workspace if workspace is not None else route_workspace(n, num_experts, te.device)
+    ws = workspace if workspace is not None else route_workspace(n, num_experts, te.device, with_gather=one_launch)
     _lib.call("moe_route_build_binned_gather", _ptr(te), _ptr(x), dt, T, H, num_experts, top_k, capacity,
               pad_multiple, _ptr(route.indices), _ptr(route.bin_ids), _ptr(route.bins), _ptr(route.padded_bins),
               _ptr(route.positions), _ptr(out), _ptr(ws), ws.numel() * 4, _ptr(status), _stream(x))
@@ -237,10 +246,12 @@ def moe_route_build_binned_gather(top_expert: torch.Tensor, x: torch.Tensor, num
 def moe_route_build_padded_gather(top_expert: torch.Tensor, x: torch.Tensor, num_experts: int, pad_multiple: int,
                                   out_rows: int | None = None, route: Route | None = None,
                                   out: torch.Tensor | None = None, workspace: torch.Tensor | None = None,
-                                  status: torch.Tensor | None = None) -> tuple[Route, torch.Tensor]:
+                                  status: torch.Tensor | None = None,
+                                  one_launch: bool = False) -> tuple[Route, torch.Tensor]:
     """Route build of top_expert [T, K] and padded gather of x [T, H] in one
     call: (route, [out_rows, H]). ``out_rows`` defaults to the bound
-    n + E*(pad_multiple-1); rows past padded_bins[-1] are zero."""
+    n + E*(pad_multiple-1); rows past padded_bins[-1] are zero. one_launch:
+    as for moe_route_build_binned_gather."""
     te = _need(top_expert, torch.int32, "top_expert")
     _need(x, None, "x", te.device)
     dt = _act_dtype(x, "x")
@@ -256,7 +267,7 @@ def moe_route_build_padded_gather(top_expert: torch.Tensor, x: torch.Tensor, num
     if out is None:
         out = torch.empty((out_rows, H), dtype=x.dtype, device=x.device)
     _need(out, x.dtype, "out", x.device)
-    ws = workspace if workspace is not None else route_workspace(n, num_experts, te.device)
+    ws = workspace if workspace is not None else route_workspace(n, num_experts, te.device, with_gather=one_launch)
     _lib.call("moe_route_build_padded_gather", _ptr(te), _ptr(x), dt, T, H, num_experts, top_k, pad_multiple,
               _ptr(route.indices), _ptr(route.bin_ids), _ptr(route.bins), _ptr(route.padded_bins),
               _ptr(route.positions), _ptr(out), out_rows, _ptr(ws), ws.numel() * 4, _ptr(status), _stream(x))

@@ -19,7 +19,7 @@ def lib():
 
 def test_header_and_exports_agree(lib):
     declared = _lib.header_functions()
-    assert len(declared) == len(set(declared)) == 20
+    assert len(declared) == len(set(declared)) == 22
     out = subprocess.run(["nm", "-D", "--defined-only", _lib.LIB_PATH], capture_output=True, text=True,
                          check=True).stdout
     exported = {ln.split()[-1] for ln in out.splitlines() if " T " in ln}
@@ -40,6 +40,8 @@ def test_informational_calls(lib):
     assert lib.moe_route_build_workspace_size(10, 0) == 0
     assert lib.moe_route_build_workspace_size(10, _lib.MOE_MAX_EXPERTS + 1) == 0
     assert lib.moe_scatter_workspace_size(65536) >= 65536 * 4
+    assert lib.moe_route_build_gather_workspace_size(65536, 256) >= lib.moe_route_build_workspace_size(65536, 256)
+    assert lib.moe_route_build_gather_workspace_size(-1, 256) == 0
 
 
 FAKE = 1 << 20  # an aligned non-null address; never dereferenced (host checks fail first)

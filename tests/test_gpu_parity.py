@@ -187,23 +187,28 @@ def test_deepseek_v3_capacity_factor_and_padding_multiple(capacity_factor, pad_m
 
 # ------------------------------------------------------------ route build + gather in one call
 
-def run_fused(r: wl.Routing, binned=True, padded=True, misalign=False):
+def run_fused(r: wl.Routing, binned=True, padded=True, misalign=False, workspace=None):
     """The one-call route build + gather against the oracle's route build and
-    gathers: all five route outputs and the gathered tensor, bit for bit."""
+    gathers: all five route outputs and the gathered tensor, bit for bit.
+    workspace None: the binding's default (the route build's size: the
+    chained launches); "one": sized for the single cooperative launch."""
     E, m = r.E, r.pad_multiple or 1
     te, x = to_dev(r.top_expert, DEV), to_dev(r.x, DEV)
     if misalign:
         x = misaligned_like(x)  # off the 16-byte rule: the register copy path
+    if workspace == "one":
+        workspace = p.ops.route_workspace(r.n, E, DEV, with_gather=True)
     o = oracle.route_build(r.top_expert, E, m)
     st = status_word()
     if binned:
-        route, xb = p.moe_route_build_binned_gather(te, x, E, r.capacity, m, status=st)
+        route, xb = p.moe_route_build_binned_gather(te, x, E, r.capacity, m, status=st, workspace=workspace)
         for k in ("indices", "bin_ids", "bins", "padded_bins", "positions"):
             assert_bits_equal(to_host(getattr(route, k)), o[k], "%s fused binned route.%s" % (r.name, k))
         o_xb = oracle.binned_gather(r.x, o["indices"], o["bin_ids"], o["bins"], E, r.capacity, r.K)
         assert_bits_equal(to_host(xb), o_xb, r.name + " fused binned_gather")
     if padded:
-        route, xp = p.moe_route_build_padded_gather(te, x, E, m, status=st)  # out_rows: the bound n + E*(m-1)
+        route, xp = p.moe_route_build_padded_gather(te, x, E, m, status=st,  # out_rows: the bound n + E*(m-1)
+                                                    workspace=workspace)
         for k in ("indices", "bin_ids", "bins", "padded_bins", "positions"):
             assert_bits_equal(to_host(getattr(route, k)), o[k], "%s fused padded route.%s" % (r.name, k))
         P = int(o["padded_bins"][-1])
@@ -228,24 +233,111 @@ def run_fused(r: wl.Routing, binned=True, padded=True, misalign=False):
     assert int(st.item()) == 0, "device status %d on valid input" % int(st.item())
 
 
-def test_fused_route_gather_tiny_and_edges():
-    run_fused(wl.pr1())
-    run_fused(wl.uniform_routing("fused-k33", 29, 24, 48, 33, wl.BF16, capacity=5, pad_multiple=8, seed=33))
-    run_fused(wl.uniform_routing("fused-h7", 37, 7, 6, 2, wl.BF16, capacity=9, pad_multiple=4, seed=7))
-    run_fused(wl.uniform_routing("fused-t1", 1, 40, 4, 2, wl.F32, capacity=1, pad_multiple=2, seed=7))
+@pytest.mark.parametrize("workspace", [None, "one"])
+def test_fused_route_gather_tiny_and_edges(workspace):
+    run_fused(wl.pr1(), workspace=workspace)
+    run_fused(wl.uniform_routing("fused-k33", 29, 24, 48, 33, wl.BF16, capacity=5, pad_multiple=8, seed=33),
+              workspace=workspace)
+    run_fused(wl.uniform_routing("fused-h7", 37, 7, 6, 2, wl.BF16, capacity=9, pad_multiple=4, seed=7),
+              workspace=workspace)
+    run_fused(wl.uniform_routing("fused-h8", 37, 8, 6, 2, wl.BF16, capacity=9, pad_multiple=4, seed=8),
+              workspace=workspace)
+    run_fused(wl.uniform_routing("fused-t1", 1, 40, 4, 2, wl.F32, capacity=1, pad_multiple=2, seed=7),
+              workspace=workspace)
     run_fused(wl.uniform_routing("fused-mis", 40, 64, 6, 2, wl.BF16, capacity=10, pad_multiple=4, seed=9),
-              misalign=True)
+              misalign=True, workspace=workspace)
     r = wl.zipf_routing("fused-cap0", 300, 40, 16, 4, wl.F32, pad_multiple=3, seed=5)
     r.capacity = 0
-    run_fused(r, padded=False)
+    run_fused(r, padded=False, workspace=workspace)
     r = wl.uniform_routing("fused-even", 64, 16, 8, 2, wl.BF16, capacity=12, pad_multiple=8, distinct=False, seed=2)
     r.top_expert = (r.top_expert // 2 * 2).astype(np.int32)  # odd experts empty
-    run_fused(r)
+    run_fused(r, workspace=workspace)
+    # more experts than threads of a CTA, many chunks per expert column
+    run_fused(wl.zipf_routing("fused-e1000", 3000, 24, 1000, 6, wl.BF16, capacity=20, pad_multiple=8, seed=4),
+              workspace=workspace)
 
 
 @pytest.mark.slow
-def test_fused_route_gather_deepseek_v3():
-    run_fused(wl.deepseek_v3())
+@pytest.mark.parametrize("workspace", [None, "one"])
+def test_fused_route_gather_deepseek_v3(workspace):
+    run_fused(wl.deepseek_v3(), workspace=workspace)
+
+
+def _kernel_names(fn):
+    """Names of the CUDA kernels `fn` launches (empty when the profiler
+    records no device activity on this platform)."""
+    from torch.profiler import ProfilerActivity, profile
+    with profile(activities=[ProfilerActivity.CUDA]) as prof:
+        fn()
+        torch.cuda.synchronize()
+    return {e.name for e in prof.events() if e.device_type == torch.autograd.DeviceType.CUDA}
+
+
+def test_one_launch_route_gather_reuses_a_garbage_workspace():
+    """With the workspace sized for it, the route build + gather call is one
+    launch of the cooperative kernel (and with the route build's workspace,
+    not); the workspace (and its barrier word) may hold anything before the
+    first call and is reused by the following calls, each bit for bit
+    against the oracle."""
+    E, m, K, T, H = 64, 8, 4, 700, 136
+    ws = p.ops.route_workspace(T * K, E, DEV, with_gather=True)
+    ws.copy_(torch.randint(-2**31, 2**31 - 1, ws.shape, dtype=torch.int64).to(torch.int32).to(DEV))
+    for seed in range(3):
+        r = wl.zipf_routing("one-launch-%d" % seed, T, H, E, K, wl.BF16, capacity=40, pad_multiple=m, seed=seed)
+        te, x = to_dev(r.top_expert, DEV), to_dev(r.x, DEV)
+        o = oracle.route_build(r.top_expert, E, m)
+        st = status_word()
+        names = _kernel_names(lambda: p.moe_route_build_padded_gather(te, x, E, m, workspace=ws, status=st))
+        if names:
+            assert any("route_gather_kernel" in n for n in names) and len(names) == 1, names
+            chained = _kernel_names(lambda: p.moe_route_build_padded_gather(te, x, E, m, status=st))
+            assert not any("route_gather_kernel" in n for n in chained) and len(chained) >= 3, chained
+        route, xp = p.moe_route_build_padded_gather(te, x, E, m, workspace=ws, status=st)
+        for k in ("indices", "bin_ids", "bins", "padded_bins", "positions"):
+            assert_bits_equal(to_host(getattr(route, k)), o[k], "one-launch route.%s" % k)
+        P = int(o["padded_bins"][-1])
+        got = to_host(xp)
+        assert_bits_equal(got[:P], oracle.padded_gather(r.x, o["indices"], o["bin_ids"], o["bins"],
+                                                        o["padded_bins"], K), "one-launch padded gather")
+        assert not got[P:].any()
+        route, xb = p.moe_route_build_binned_gather(te, x, E, r.capacity, m, workspace=ws, status=st)
+        assert_bits_equal(to_host(xb), oracle.binned_gather(r.x, o["indices"], o["bin_ids"], o["bins"], E,
+                                                            r.capacity, K), "one-launch binned gather")
+        torch.cuda.synchronize()
+        assert int(st.item()) == 0
+
+
+def test_one_launch_bad_expert_ids_are_reported():
+    E, K, T, H = 16, 2, 300, 64
+    r = wl.uniform_routing("one-launch-bad", T, H, E, K, wl.BF16, capacity=50, pad_multiple=4, seed=3)
+    te_h = r.top_expert.copy()
+    te_h.reshape(-1)[[5, 77, 401]] = [-1, E, 1 << 20]
+    te, x = to_dev(te_h, DEV), to_dev(r.x, DEV)
+    st = status_word()
+    route, _ = p.moe_route_build_padded_gather(te, x, E, 4, status=st, one_launch=True)
+    torch.cuda.synchronize()
+    assert int(st.item()) & _lib.MOE_STATUS_BAD_EXPERT
+    pos = to_host(route.positions)
+    assert (pos[[5, 77, 401]] == -1).all()
+
+
+def test_one_launch_barrier_timeout_is_reported():
+    """Every grid barrier of the one-launch path is a bounded wait: with its
+    target raised past the number of CTAs (the testing hook), each CTA gives
+    up, sets MOE_STATUS_TIMEOUT and stops; the device stays usable and the
+    next call is exact again."""
+    lib = _lib.load()
+    r = wl.uniform_routing("one-launch-timeout", 200, 64, 8, 2, wl.BF16, capacity=60, pad_multiple=4, seed=1)
+    te, x = to_dev(r.top_expert, DEV), to_dev(r.x, DEV)
+    st = status_word()
+    lib.moe_test_barrier_slack(1)
+    try:
+        p.moe_route_build_padded_gather(te, x, r.E, 4, status=st, one_launch=True)
+        torch.cuda.synchronize()
+    finally:
+        lib.moe_test_barrier_slack(0)
+    assert int(st.item()) & _lib.MOE_STATUS_TIMEOUT
+    run_fused(r, workspace="one")
 
 
 # ------------------------------------------------------------ edge matrix

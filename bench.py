@@ -913,8 +913,9 @@ def run_profile_case(args):
     `--profile-ops` once more, in that order, so that an ncu capture with
     `-k <kernel> -s <launches of that kernel in the warm-up pass>` sees
     exactly the second pass. Besides the step's ops (and the next rows'
-    `topk_gating`, and `binned_gather_weighted` / `padded_gather_weighted`
-    when one of them is named), `qwen_compaction_fwd` / `qwen_compaction_bwd` run the
+    `topk_gating`, `binned_gather_weighted` / `padded_gather_weighted` when
+    one of them is named, and `route_build_binned_gather_one_launch` /
+    `route_build_padded_gather_one_launch` likewise), `qwen_compaction_fwd` / `qwen_compaction_bwd` run the
     compaction on its own Qwen2-MoE-57B-shaped map (T=65536, E=64, topk=8),
     once as warm-up and once more when named."""
     import torch
@@ -940,6 +941,10 @@ def run_profile_case(args):
         ops["padded_gather_weighted"] = lambda: path.p.moe_padded_gather_weighted(
             path.grad, rt.indices, rt.bins, rt.padded_bins, w, r.K, out_rows=path.P, out=gwp,
             positions=rt.positions)
+    if any(name.endswith("_one_launch") for name in args.profile_ops.split(",")):
+        for name, f, _ in path.next_ops():
+            if name.endswith("_one_launch"):
+                ops[name] = f
     ops["qwen_compaction_fwd"] = lambda: path.p.moe_routing_map_to_indices_fwd(qp, qm, q.topk, out=(qpi, qidx))
     ops["qwen_compaction_bwd"] = lambda: path.p.moe_routing_map_to_indices_bwd(qg, qidx, q.probs.shape[1], out=qgp)
     for name in ops:

@@ -578,7 +578,11 @@ __global__ void __launch_bounds__(tma_threads<PADDED>(), 1) gather_tma_kernel(Ga
 // upper 48 bits carry a per-call tag, so the word needs no initialisation
 // (a stale value from an earlier call is re-tagged by the first arrival);
 // each wait is bounded and a CTA that gives up sets MOE_STATUS_TIMEOUT and
-// leaves, so every CTA ends.
+// leaves, so every CTA ends. The caller opts in through the workspace size:
+// at the DeepSeek-V3 shape, 16 to 8192 tokens, it measured slower than the
+// route build's launches chained to the token pass (8192 tokens: binned
+// 0.191 vs 0.187 ms, padded 0.237 vs 0.231; 16 tokens: 24.6 vs 17.9 us),
+// each barrier costing 2-3 us across the grid, more than a chained launch.
 
 struct RouteGatherArgs {
   const int32_t* top_expert;

@@ -576,9 +576,10 @@ __global__ void __launch_bounds__(tma_threads<PADDED>(), 1) gather_tma_kernel(Ga
 //   C  the bulk-copy token pass, reading those positions (coherent loads).
 // The barrier counts CTA arrivals in one 64-bit word of the workspace whose
 // upper 48 bits carry a per-call tag, so the word needs no initialisation
-// (a stale value from an earlier call is re-tagged by the first arrival);
-// each wait is bounded and a CTA that gives up sets MOE_STATUS_TIMEOUT and
-// leaves, so every CTA ends. The caller opts in through the workspace size:
+// (a stale value from an earlier call is re-tagged by the first arrival,
+// and the last CTA to leave clears it, so a CUDA graph replaying the launch
+// with the same tag starts from zero); each wait is bounded and a CTA that
+// gives up sets MOE_STATUS_TIMEOUT and leaves, so every CTA ends. The caller opts in through the workspace size:
 // at the DeepSeek-V3 shape, 16 to 8192 tokens, it measured slower than the
 // route build's launches chained to the token pass (8192 tokens: binned
 // 0.191 vs 0.187 ms, padded 0.237 vs 0.231; 16 tokens: 24.6 vs 17.9 us),
@@ -607,38 +608,63 @@ __device__ __forceinline__ unsigned long long ld_acquire_u64(const unsigned long
   return v;
 }
 
-// Arrive at the grid barrier and wait until `target` CTAs of this call have
-// arrived (bounded). Every thread of the CTA calls it; all get the result.
-__device__ bool grid_barrier(const RouteGatherArgs& f, uint32_t target, int32_t* status) {
+// Arrival b (1, 2, 3) at the grid barrier of a launch of `grid` CTAs: waits
+// (bounded) until every CTA of this call has arrived b times, plus `slack`
+// (testing). The word's low 15 bits count arrivals; bit 15 marks a failed
+// launch: a CTA that gives up sets it, so a later launch with the same tag
+// (a CUDA graph replayed after a failure) cannot take the stale count for
+// its own and stops too. An arrival that finds the count outside this
+// barrier's window stops likewise. Stopping sets MOE_STATUS_TIMEOUT. Every
+// thread of the CTA calls it; all get the result.
+constexpr unsigned long long kFailedBit = 0x8000ull;
+__device__ bool grid_barrier(const RouteGatherArgs& f, uint32_t b, uint32_t grid, int32_t* status) {
   __shared__ int passed;
   __syncthreads();
   if (threadIdx.x == 0) {
     __threadfence();  // this CTA's writes before its arrival
-    bool arrived = false;
+    bool arrived = false, in_window = false;
     for (int it = 0; it < 4096 && !arrived; ++it) {
       const unsigned long long cur = ld_acquire_u64(f.barrier);
       if ((cur & kTagMask) == f.tag) {
-        atomicAdd(f.barrier, 1ull);
+        const uint32_t before = (uint32_t)(atomicAdd(f.barrier, 1ull) & 0xffffull);
+        in_window = before >= (b - 1) * grid && before < b * grid;  // the failed bit is outside every window
         arrived = true;
       } else if (atomicCAS(f.barrier, cur, f.tag | 1ull) == cur) {
-        arrived = true;  // first arrival of this call: the word is re-tagged
+        in_window = b == 1;  // first arrival of this call: the word is re-tagged
+        arrived = true;
       }
     }
     bool ok = false;
-    for (int it = 0; arrived && it < kSpinLimit; ++it) {
+    const uint32_t target = b * grid + f.slack;
+    for (int it = 0; arrived && in_window && it < kSpinLimit; ++it) {
       const unsigned long long cur = ld_acquire_u64(f.barrier);
-      if ((cur & kTagMask) == f.tag && (uint32_t)(cur & 0xffffull) >= target) {
+      if ((cur & kTagMask) != f.tag || (cur & kFailedBit)) break;
+      if ((uint32_t)(cur & 0xffffull) >= target) {
         ok = true;
         break;
       }
       __nanosleep(64);
     }
-    if (!ok) flag_status(status, MOE_STATUS_TIMEOUT);
+    if (!ok) {
+      flag_status(status, MOE_STATUS_TIMEOUT);
+      if (arrived) atomicOr(f.barrier, kFailedBit);
+    }
     __threadfence();
     passed = ok;
   }
   __syncthreads();
   return passed != 0;
+}
+
+// After the last barrier: the CTA whose departure completes the count
+// clears the word, so that a later launch with the same tag (a CUDA graph
+// replayed) starts from zero. Every CTA has passed the last barrier by then.
+__device__ void grid_depart(const RouteGatherArgs& f, uint32_t barriers, uint32_t grid) {
+  if (threadIdx.x == 0) {
+    const unsigned long long before = atomicAdd(f.barrier, 1ull);
+    if ((before & kTagMask) == f.tag && (uint32_t)(before & 0xffffull) == (barriers + 1) * grid - 1)
+      atomicExch(f.barrier, 0ull);
+  }
 }
 
 // Exclusive scan over experts of v[e] (in place) and of its rounding up to
@@ -728,7 +754,7 @@ __global__ void __launch_bounds__(tma_threads<PADDED>(), 1)
     for (int w = 0; w < kWarpsCta; ++w) c += whist[w * E + e];
     f.counts[(int64_t)blockIdx.x * E + e] = c;
   }
-  if (!grid_barrier(f, (uint32_t)G + f.slack, g.status)) return;
+  if (!grid_barrier(f, 1, (uint32_t)G, g.status)) return;
 
   // B1: a warp per expert: exclusive prefix of its column over the chunks,
   // kColPer chunks per lane loaded at once and held in registers.
@@ -760,7 +786,7 @@ __global__ void __launch_bounds__(tma_threads<PADDED>(), 1)
     }
     if (lane == 0) totals[e] = carry;
   }
-  if (!grid_barrier(f, (uint32_t)(2 * G) + f.slack, g.status)) return;
+  if (!grid_barrier(f, 2, (uint32_t)G, g.status)) return;
 
   // B2: bins from the totals, then this chunk's sorted positions.
   for (int e = threadIdx.x; e < E; e += blockDim.x) {
@@ -802,15 +828,21 @@ __global__ void __launch_bounds__(tma_threads<PADDED>(), 1)
     const unsigned peers = __match_any_sync(kAll, e);
     if (e >= 0) {
       const int32_t dst = mine[e] + __popc(peers & lt);
-      f.indices[dst] = (int32_t)a;
-      f.bin_ids[dst] = e;
-      f.positions[a] = dst;
+      if (dst >= 0 && dst < g.n) {
+        f.indices[dst] = (int32_t)a;
+        f.bin_ids[dst] = e;
+        f.positions[a] = dst;
+      } else {
+        flag_status(g.status, MOE_STATUS_BAD_BINS);  // only on a broken barrier
+        f.positions[a] = -1;
+      }
     }
     __syncwarp();
     if (e >= 0 && lane == __ffs(peers) - 1) mine[e] += __popc(peers);
     __syncwarp();
   }
-  if (!grid_barrier(f, (uint32_t)(3 * G) + f.slack, g.status)) return;
+  if (!grid_barrier(f, 3, (uint32_t)G, g.status)) return;
+  grid_depart(f, 3, (uint32_t)G);
 
   // C: the token pass over the positions just written.
   tma_copy_pass<PADDED, true>(g, row_bytes, sbins, PADDED ? spbins : nullptr, tsm);
@@ -846,7 +878,7 @@ int64_t route_gather_grid() {
     return 0;
   }
   const int64_t grid = (int64_t)per_sm * num_sms();
-  return grid * 3 <= 0xffff ? grid : 0;  // three barriers' arrivals fit the word's 16-bit count
+  return grid * 4 < (int64_t)kFailedBit ? grid : 0;  // three barriers' arrivals and the departures fit the count bits
 }
 
 // Workspace of the one-launch path: the [grid][E] count matrix and [E]

@@ -307,6 +307,55 @@ def test_one_launch_route_gather_reuses_a_garbage_workspace():
         assert int(st.item()) == 0
 
 
+def test_one_launch_route_gather_replays_from_a_cuda_graph():
+    """The one-launch call captured in a CUDA graph: every replay reuses the
+    captured barrier tag, so each launch must leave the barrier word clear
+    for the next. Three replays, new routing written into the captured input
+    before each, each bit for bit against the oracle."""
+    E, m, K, T, H = 32, 4, 4, 400, 64
+    n, out_rows = T * K, T * K + E * (m - 1)
+    rs = [wl.zipf_routing("graph-%d" % sd, T, H, E, K, wl.BF16, pad_multiple=m, seed=sd) for sd in range(3)]
+    x = to_dev(rs[0].x, DEV)  # the token rows stay; the routing changes between replays
+    te = to_dev(rs[0].top_expert, DEV)
+    ws = p.ops.route_workspace(n, E, DEV, with_gather=True)
+    route = p.Route(*(torch.empty(k, dtype=torch.int32, device=DEV) for k in (n, n, E, E, n)))
+    xp = torch.empty((out_rows, H), dtype=x.dtype, device=DEV)
+    st = status_word()
+
+    def call():
+        p.moe_route_build_padded_gather(te, x, E, m, out_rows=out_rows, route=route, out=xp, workspace=ws,
+                                        status=st)
+
+    side = torch.cuda.Stream(DEV)
+    side.wait_stream(torch.cuda.current_stream(DEV))
+    with torch.cuda.stream(side):
+        call()  # warm-up on the capture stream's side, as torch asks
+    torch.cuda.current_stream(DEV).wait_stream(side)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        call()
+    for i, r in enumerate(rs):
+        te.copy_(to_dev(r.top_expert, DEV))
+        xp.fill_(float("nan"))
+        if i == 0:
+            names = _kernel_names(graph.replay)
+            if names:
+                assert any("route_gather_kernel" in nm for nm in names), names
+        else:
+            graph.replay()
+        torch.cuda.synchronize()
+        o = oracle.route_build(r.top_expert, E, m)
+        for k in ("indices", "bin_ids", "bins", "padded_bins", "positions"):
+            assert_bits_equal(to_host(getattr(route, k)), o[k], "graph replay %d route.%s" % (i, k))
+        P = int(o["padded_bins"][-1])
+        got = to_host(xp)
+        assert_bits_equal(got[:P], oracle.padded_gather(rs[0].x, o["indices"], o["bin_ids"], o["bins"],
+                                                        o["padded_bins"], K), "graph replay %d gather" % i)
+        assert not got[P:].any()
+        assert int(st.item()) == 0, "replay %d status %d" % (i, int(st.item()))
+
+
 def test_one_launch_bad_expert_ids_are_reported():
     E, K, T, H = 16, 2, 300, 64
     r = wl.uniform_routing("one-launch-bad", T, H, E, K, wl.BF16, capacity=50, pad_multiple=4, seed=3)

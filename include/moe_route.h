@@ -265,7 +265,10 @@ int moe_padded_gather_weighted(const void* dy, int32_t dtype,
  *   that gives up sets MOE_STATUS_TIMEOUT and stops (outputs then
  *   unspecified). The barrier word in the workspace needs no
  *   initialisation, but two such calls must not use one workspace at the
- *   same time. Otherwise three or four launches (the route build's two or
+ *   same time. A CUDA graph may capture the call and replay it (each
+ *   launch leaves the word clear for the next); after a timeout the word
+ *   stays marked, so replays of that captured launch keep reporting
+ *   MOE_STATUS_TIMEOUT until a new call (or a new capture) is made. Otherwise three or four launches (the route build's two or
  *   three and the gather's token pass, chained by programmatic dependent
  *   launch), needing only moe_route_build_workspace_size(n, E) bytes of
  *   workspace. On GB300 the chained launches measured faster at every batch

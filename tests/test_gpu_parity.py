@@ -263,14 +263,13 @@ def test_fused_route_gather_deepseek_v3(workspace):
     run_fused(wl.deepseek_v3(), workspace=workspace)
 
 
-def _kernel_names(fn):
-    """Names of the CUDA kernels `fn` launches (empty when the profiler
-    records no device activity on this platform)."""
-    from torch.profiler import ProfilerActivity, profile
-    with profile(activities=[ProfilerActivity.CUDA]) as prof:
-        fn()
-        torch.cuda.synchronize()
-    return {e.name for e in prof.events() if e.device_type == torch.autograd.DeviceType.CUDA}
+def _untouched(ws):
+    """Fraction of a workspace's int32 words still holding the fill -1: the
+    one-launch kernel writes its whole count matrix (non-negative counts),
+    the chained route build only its own few chunks' counts (under 1 % of a
+    workspace sized for the one launch), so this tells which form ran."""
+    torch.cuda.synchronize()
+    return float((ws == -1).float().mean().item())
 
 
 def test_one_launch_route_gather_reuses_a_garbage_workspace():
@@ -287,11 +286,10 @@ def test_one_launch_route_gather_reuses_a_garbage_workspace():
         te, x = to_dev(r.top_expert, DEV), to_dev(r.x, DEV)
         o = oracle.route_build(r.top_expert, E, m)
         st = status_word()
-        names = _kernel_names(lambda: p.moe_route_build_padded_gather(te, x, E, m, workspace=ws, status=st))
-        if names:
-            assert any("route_gather_kernel" in n for n in names) and len(names) == 1, names
-            chained = _kernel_names(lambda: p.moe_route_build_padded_gather(te, x, E, m, status=st))
-            assert not any("route_gather_kernel" in n for n in chained) and len(chained) >= 3, chained
+        if seed == 0:  # which form runs: the one-launch kernel fills its whole count matrix
+            probe = torch.full_like(ws, -1)
+            p.moe_route_build_padded_gather(te, x, E, m, workspace=probe, status=st)
+            assert _untouched(probe) < 0.5  # the chained route build would write well under 1 % of it
         route, xp = p.moe_route_build_padded_gather(te, x, E, m, workspace=ws, status=st)
         for k in ("indices", "bin_ids", "bins", "padded_bins", "positions"):
             assert_bits_equal(to_host(getattr(route, k)), o[k], "one-launch route.%s" % k)
@@ -335,15 +333,11 @@ def test_one_launch_route_gather_replays_from_a_cuda_graph():
     graph = torch.cuda.CUDAGraph()
     with torch.cuda.graph(graph):
         call()
+    ws.fill_(-1)
     for i, r in enumerate(rs):
         te.copy_(to_dev(r.top_expert, DEV))
         xp.fill_(float("nan"))
-        if i == 0:
-            names = _kernel_names(graph.replay)
-            if names:
-                assert any("route_gather_kernel" in nm for nm in names), names
-        else:
-            graph.replay()
+        graph.replay()
         torch.cuda.synchronize()
         o = oracle.route_build(r.top_expert, E, m)
         for k in ("indices", "bin_ids", "bins", "padded_bins", "positions"):
@@ -354,6 +348,7 @@ def test_one_launch_route_gather_replays_from_a_cuda_graph():
                                                         o["padded_bins"], K), "graph replay %d gather" % i)
         assert not got[P:].any()
         assert int(st.item()) == 0, "replay %d status %d" % (i, int(st.item()))
+        assert _untouched(ws) < 0.5  # the replays ran the one-launch kernel
 
 
 def test_one_launch_bad_expert_ids_are_reported():

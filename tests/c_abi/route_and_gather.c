@@ -2,8 +2,12 @@
  * A plain C host of the routing library: no Python, no torch. It allocates
  * device memory with the CUDA runtime, runs moe_route_build and then
  * moe_binned_gather / moe_padded_gather / moe_binned_scatter through the C
- * ABI of include/moe_route.h on a seeded problem, and writes the inputs and
- * every output to a binary file for the test to compare with the oracle.
+ * ABI of include/moe_route.h on a seeded problem, then the route build +
+ * padded gather in one launch (workspace of
+ * moe_route_build_gather_workspace_size bytes, filled with 0xff first so
+ * that the test can see the launch wrote its count matrix), and writes the
+ * inputs and every output to a binary file for the test to compare with the
+ * oracle.
  *
  *   route_and_gather OUT.bin
  */
@@ -95,12 +99,46 @@ int main(int argc, char** argv) {
   CHECK_CUDA(cudaMemcpy(y, d_y, T * H * 4, cudaMemcpyDeviceToHost));
   CHECK_CUDA(cudaMemcpy(&status, d_status, 4, cudaMemcpyDeviceToHost));
 
+  /* route build + padded gather in one call, sized for the single launch */
+  const size_t ws1 = moe_route_build_gather_workspace_size(n, E);
+  const int64_t out_rows = n + (int64_t)E * (m - 1); /* the bound: no read-back needed */
+  int32_t *d_idx1, *d_bid1, *d_bins1, *d_pb1, *d_pos1;
+  float* d_xp1;
+  void* d_ws1;
+  CHECK_CUDA(cudaMalloc((void**)&d_idx1, n * 4));
+  CHECK_CUDA(cudaMalloc((void**)&d_bid1, n * 4));
+  CHECK_CUDA(cudaMalloc((void**)&d_pos1, n * 4));
+  CHECK_CUDA(cudaMalloc((void**)&d_bins1, E * 4));
+  CHECK_CUDA(cudaMalloc((void**)&d_pb1, E * 4));
+  CHECK_CUDA(cudaMalloc((void**)&d_xp1, out_rows * H * 4));
+  CHECK_CUDA(cudaMalloc(&d_ws1, ws1));
+  CHECK_CUDA(cudaMemset(d_ws1, 0xff, ws1));
+  CHECK_MOE(moe_route_build_padded_gather(d_te, d_x, MOE_F32, T, H, E, K, m, d_idx1, d_bid1, d_bins1, d_pb1, d_pos1,
+                                          d_xp1, out_rows, d_ws1, ws1, d_status, s));
+  CHECK_CUDA(cudaStreamSynchronize(s));
+  int32_t *idx1 = malloc(n * 4), *bid1 = malloc(n * 4), *pos1 = malloc(n * 4), *bins1 = malloc(E * 4),
+          *pb1 = malloc(E * 4), *wsh = malloc(ws1);
+  float* xp1 = malloc(out_rows * H * 4);
+  CHECK_CUDA(cudaMemcpy(idx1, d_idx1, n * 4, cudaMemcpyDeviceToHost));
+  CHECK_CUDA(cudaMemcpy(bid1, d_bid1, n * 4, cudaMemcpyDeviceToHost));
+  CHECK_CUDA(cudaMemcpy(pos1, d_pos1, n * 4, cudaMemcpyDeviceToHost));
+  CHECK_CUDA(cudaMemcpy(bins1, d_bins1, E * 4, cudaMemcpyDeviceToHost));
+  CHECK_CUDA(cudaMemcpy(pb1, d_pb1, E * 4, cudaMemcpyDeviceToHost));
+  CHECK_CUDA(cudaMemcpy(xp1, d_xp1, out_rows * H * 4, cudaMemcpyDeviceToHost));
+  CHECK_CUDA(cudaMemcpy(wsh, d_ws1, ws1, cudaMemcpyDeviceToHost));
+  CHECK_CUDA(cudaMemcpy(&status, d_status, 4, cudaMemcpyDeviceToHost));
+  int64_t untouched = 0; /* words still 0xffffffff */
+  for (size_t i = 0; i < ws1 / 4; ++i) untouched += wsh[i] == -1;
+
   FILE* f = fopen(argv[1], "wb");
   if (f == NULL) return 4;
   const int64_t header[8] = {T, H, E, K, m, cap, P, status};
   int bad = put(f, header, sizeof(header)) | put(f, te, n * 4) | put(f, x, T * H * 4) | put(f, idx, n * 4) |
             put(f, bid, n * 4) | put(f, bins, E * 4) | put(f, pb, E * 4) | put(f, pos, n * 4) |
             put(f, xb, (size_t)E * cap * H * 4) | put(f, xp, P * H * 4) | put(f, y, T * H * 4);
+  const int64_t tail[3] = {out_rows, (int64_t)(ws1 / 4), untouched};
+  bad |= put(f, tail, sizeof(tail)) | put(f, idx1, n * 4) | put(f, bid1, n * 4) | put(f, bins1, E * 4) |
+         put(f, pb1, E * 4) | put(f, pos1, n * 4) | put(f, xp1, out_rows * H * 4);
   fclose(f);
   printf("moe_version %d, status %d, padded rows %lld\n", moe_version(), status, (long long)P);
   return bad ? 5 : 0;

@@ -1,8 +1,9 @@
 """The C ABI from a plain C host (tests/c_abi/route_and_gather.c, built with
 gcc against include/moe_route.h, libmoe_route.so and the CUDA runtime, no
 Python or torch in the process): route build, binned and padded gather and
-the unweighted binned scatter on a seeded problem, every output compared
-with the oracle bit for bit."""
+the unweighted binned scatter on a seeded problem, then the route build +
+padded gather in one launch, every output compared with the oracle bit for
+bit."""
 import os
 import shutil
 import subprocess
@@ -55,6 +56,10 @@ def test_plain_c_host_matches_the_oracle(tmp_path):
     xb = take(E * cap * H, np.float32).reshape(E, cap, H)
     xp = take(P * H, np.float32).reshape(P, H)
     y = take(T * H, np.float32).reshape(T, H)
+    out_rows, ws_words, untouched = take(3, np.int64)
+    got1 = {k: take(n if k not in ("bins", "padded_bins") else E, np.int32)
+            for k in ("indices", "bin_ids", "bins", "padded_bins", "positions")}
+    xp1 = take(out_rows * H, np.float32).reshape(out_rows, H)
     assert off == len(raw) and status == 0
     o = oracle.route_build(te, int(E), int(m))
     for k, v in got.items():
@@ -65,3 +70,9 @@ def test_plain_c_host_matches_the_oracle(tmp_path):
     assert np.array_equal(xp.view(np.uint32), o_xp.view(np.uint32))
     o_y = oracle.binned_scatter(o_xb, o["indices"], o["bin_ids"], o["bins"], None, int(T), int(K))
     assert np.array_equal(y.view(np.uint32), o_y.view(np.uint32))
+    # the one-launch call: same route, the gather's rows, zeros past padded_bins[-1]
+    for k, v in got1.items():
+        assert np.array_equal(v, o[k]), "one launch " + k
+    assert out_rows >= P and np.array_equal(xp1[:P].view(np.uint32), o_xp.view(np.uint32))
+    assert not xp1[P:].any()
+    assert untouched < ws_words // 2  # the single launch wrote its count matrix over the 0xff fill

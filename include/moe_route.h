@@ -70,8 +70,9 @@ enum moe_device_status {
                                    entry that indices does not map back (indices[positions[a]] != a) */
   MOE_STATUS_BAD_BINS = 4,     /* bins / padded_bins not monotonic or not consistent */
   MOE_STATUS_ROWS_MISMATCH = 8, /* padded_bins[E-1] exceeds the rows the caller provided */
-  MOE_STATUS_TIMEOUT = 16       /* a bounded wait on an asynchronous copy gave up: the launch's
-                                   outputs are unspecified and the stream must be
+  MOE_STATUS_TIMEOUT = 16       /* a bounded wait gave up (on an asynchronous copy, or at a grid
+                                   barrier of the one-launch route build + gather): the
+                                   launch's outputs are unspecified and the stream must be
                                    treated as failed (a copy may still be landing) */
 };
 
@@ -268,10 +269,10 @@ int moe_padded_gather_weighted(const void* dy, int32_t dtype,
  *   same time. A CUDA graph may capture the call and replay it (each
  *   launch leaves the word clear for the next); after a timeout the word
  *   stays marked, so replays of that captured launch keep reporting
- *   MOE_STATUS_TIMEOUT until a new call (or a new capture) is made. Otherwise three or four launches (the route build's two or
- *   three and the gather's token pass, chained by programmatic dependent
- *   launch), needing only moe_route_build_workspace_size(n, E) bytes of
- *   workspace. On GB300 the chained launches measured faster at every batch
+ *   MOE_STATUS_TIMEOUT until a new call (or a new capture) is made.
+ *   Otherwise three or four launches (the route build's two or three and
+ *   the gather's token pass, chained by programmatic dependent launch),
+ *   needing only moe_route_build_workspace_size(n, E) bytes of workspace. On GB300 the chained launches measured faster at every batch
  *   size tried (16 to 8192 tokens of the DeepSeek-V3 shape: the single
  *   launch's three grid barriers cost more than the launches they replace),
  *   so the larger workspace is for callers that want exactly one kernel.

@@ -67,7 +67,8 @@ enum moe_dtype { MOE_F32 = 0, MOE_BF16 = 1 };
 enum moe_device_status {
   MOE_STATUS_BAD_EXPERT = 1,   /* expert id outside [0, E) */
   MOE_STATUS_BAD_INDEX = 2,    /* an index or position outside its range, or a positions
-                                   entry that indices does not map back (indices[positions[a]] != a) */
+                                   entry that indices does not map back
+                                   (indices[positions[a]] != a) */
   MOE_STATUS_BAD_BINS = 4,     /* bins / padded_bins not monotonic or not consistent */
   MOE_STATUS_ROWS_MISMATCH = 8, /* padded_bins[E-1] exceeds the rows the caller provided */
   MOE_STATUS_TIMEOUT = 16       /* a bounded wait gave up (on an asynchronous copy, or at a grid
@@ -272,10 +273,11 @@ int moe_padded_gather_weighted(const void* dy, int32_t dtype,
  *   MOE_STATUS_TIMEOUT until a new call (or a new capture) is made.
  *   Otherwise three or four launches (the route build's two or three and
  *   the gather's token pass, chained by programmatic dependent launch),
- *   needing only moe_route_build_workspace_size(n, E) bytes of workspace. On GB300 the chained launches measured faster at every batch
- *   size tried (16 to 8192 tokens of the DeepSeek-V3 shape: the single
- *   launch's three grid barriers cost more than the launches they replace),
- *   so the larger workspace is for callers that want exactly one kernel.
+ *   needing only moe_route_build_workspace_size(n, E) bytes of workspace.
+ *   On GB300 the chained launches measured faster at every batch size tried
+ *   (16 to 8192 tokens of the DeepSeek-V3 shape: the single launch's three
+ *   grid barriers cost more than the launches they replace), so the larger
+ *   workspace is for callers that want exactly one kernel.
  *   padded: out has out_rows rows; the caller does not know
  *   padded_bins[E-1] before the call, so out_rows is a bound, such as
  *   n + E*(pad_multiple-1) (every padded total is at most that); rows at

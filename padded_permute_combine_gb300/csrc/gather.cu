@@ -582,7 +582,7 @@ __global__ void __launch_bounds__(tma_threads<PADDED>(), 1) gather_tma_kernel(Ga
 // gives up sets MOE_STATUS_TIMEOUT and leaves, so every CTA ends. The caller opts in through the workspace size:
 // at the DeepSeek-V3 shape, 16 to 8192 tokens, it measured slower than the
 // route build's launches chained to the token pass (8192 tokens: binned
-// 0.191 vs 0.187 ms, padded 0.237 vs 0.231; 16 tokens: 24.6 vs 17.9 us),
+// 0.191 vs 0.185 ms, padded 0.236 vs 0.228; 16 tokens: 22.5 vs 17.9 us),
 // each barrier costing 2-3 us across the grid, more than a chained launch.
 
 struct RouteGatherArgs {
@@ -899,20 +899,26 @@ bool launch_route_gather(const GatherArgs& g, int64_t row_bytes, RouteGatherArgs
                          size_t workspace_bytes, cudaStream_t s, int* rc) {
   if (!MOE_GATHER_TMA || row_bytes % 16 != 0 || !aligned(g.x, 16) || !aligned(g.out, 16)) return false;
   if (g.E > kStageMax || g.n < 1 || g.rows_out < 1 || !aligned(workspace, 8)) return false;
-  const int64_t grid = route_gather_grid<PADDED>();
-  if (grid < 1 || workspace_bytes < route_gather_workspace(grid, g.E)) return false;
+  GatherArgs gt = g;
+  gt.row_begin = gt.rows_out;
+  gt.segs = MOE_TMA_SEGS;
+  gt.seg_len = ((row_bytes + gt.segs - 1) / gt.segs + 15) / 16 * 16;  // bytes, 16-byte multiples
+  gt.segs = (row_bytes + gt.seg_len - 1) / gt.seg_len;
+  // As many CTAs as the token pass has work for (a copy warp per token
+  // segment), at most all that fit at once and at least one per SM (the
+  // zero rows, most of a small batch's padded output, need that many bulk-
+  // store issuers): the grid barriers cost less on a smaller grid.
+  const int64_t resident = route_gather_grid<PADDED>();
+  const int64_t work = (gt.T * gt.segs + kTmaWarps - 1) / kTmaWarps;
+  const int64_t grid = min(resident, max((int64_t)num_sms(), work));
+  if (resident < 1 || workspace_bytes < route_gather_workspace(grid, g.E)) return false;
   f.counts = static_cast<int32_t*>(workspace);
   f.barrier = reinterpret_cast<unsigned long long*>(static_cast<char*>(workspace) +
                                                     route_gather_workspace(grid, g.E) - 8);
   f.tag = ((g_route_gather_calls.fetch_add(1, std::memory_order_relaxed) + 1) & 0xffffffffffffull) << 16;
   f.chunk = (g.n + grid - 1) / grid;
   f.slack = g_barrier_slack.load(std::memory_order_relaxed);
-  GatherArgs gt = g;
   gt.positions = f.positions;
-  gt.row_begin = gt.rows_out;
-  gt.segs = MOE_TMA_SEGS;
-  gt.seg_len = ((row_bytes + gt.segs - 1) / gt.segs + 15) / 16 * 16;  // bytes, 16-byte multiples
-  gt.segs = (row_bytes + gt.seg_len - 1) / gt.seg_len;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)grid);
   cfg.blockDim = dim3(tma_threads<PADDED>());

@@ -75,4 +75,6 @@ def test_plain_c_host_matches_the_oracle(tmp_path):
         assert np.array_equal(v, o[k]), "one launch " + k
     assert out_rows >= P and np.array_equal(xp1[:P].view(np.uint32), o_xp.view(np.uint32))
     assert not xp1[P:].any()
-    assert untouched < ws_words // 2  # the single launch wrote its count matrix over the 0xff fill
+    # the single launch wrote its count matrix (a row per CTA) over the 0xff fill; the chained
+    # route build would have written at most its own workspace's words
+    assert ws_words - untouched > _lib.load().moe_route_build_workspace_size(int(n), int(E)) // 4

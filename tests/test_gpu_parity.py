@@ -263,13 +263,13 @@ def test_fused_route_gather_deepseek_v3(workspace):
     run_fused(wl.deepseek_v3(), workspace=workspace)
 
 
-def _untouched(ws):
-    """Fraction of a workspace's int32 words still holding the fill -1: the
-    one-launch kernel writes its whole count matrix (non-negative counts),
-    the chained route build only its own few chunks' counts (under 1 % of a
-    workspace sized for the one launch), so this tells which form ran."""
+def _written(ws):
+    """int32 words of a workspace no longer holding the fill -1: the one-launch
+    kernel writes a count matrix of one row per CTA (non-negative counts),
+    the chained route build at most its own workspace's words, so more than
+    that tells that the single launch ran."""
     torch.cuda.synchronize()
-    return float((ws == -1).float().mean().item())
+    return int((ws != -1).sum().item())
 
 
 def test_one_launch_route_gather_reuses_a_garbage_workspace():
@@ -289,7 +289,7 @@ def test_one_launch_route_gather_reuses_a_garbage_workspace():
         if seed == 0:  # which form runs: the one-launch kernel fills its whole count matrix
             probe = torch.full_like(ws, -1)
             p.moe_route_build_padded_gather(te, x, E, m, workspace=probe, status=st)
-            assert _untouched(probe) < 0.5  # the chained route build would write well under 1 % of it
+            assert _written(probe) > p.ops.route_workspace(T * K, E, DEV).numel()
         route, xp = p.moe_route_build_padded_gather(te, x, E, m, workspace=ws, status=st)
         for k in ("indices", "bin_ids", "bins", "padded_bins", "positions"):
             assert_bits_equal(to_host(getattr(route, k)), o[k], "one-launch route.%s" % k)
@@ -348,7 +348,7 @@ def test_one_launch_route_gather_replays_from_a_cuda_graph():
                                                         o["padded_bins"], K), "graph replay %d gather" % i)
         assert not got[P:].any()
         assert int(st.item()) == 0, "replay %d status %d" % (i, int(st.item()))
-        assert _untouched(ws) < 0.5  # the replays ran the one-launch kernel
+        assert _written(ws) > p.ops.route_workspace(n, E, DEV).numel()  # the replays ran the one launch
 
 
 def test_one_launch_bad_expert_ids_are_reported():

@@ -351,6 +351,39 @@ def test_one_launch_route_gather_replays_from_a_cuda_graph():
         assert _written(ws) > p.ops.route_workspace(n, E, DEV).numel()  # the replays ran the one launch
 
 
+def test_one_launch_route_gather_beside_other_streams():
+    """The one-launch call enqueued while another stream runs a large padded
+    gather and scatter: its CTAs may only become resident as the other
+    kernels drain, which the bounded barriers outlast; every call exact,
+    status clear."""
+    big = wl.deepseek_v3()
+    bx = to_dev(big.x, DEV)
+    bte = to_dev(big.top_expert, DEV)
+    brt = p.moe_route_build(bte, big.E, big.pad_multiple)
+    torch.cuda.synchronize()
+    E, m, K, T, H = 64, 8, 4, 700, 136
+    r = wl.zipf_routing("one-launch-busy", T, H, E, K, wl.BF16, capacity=40, pad_multiple=m, seed=9)
+    te, x = to_dev(r.top_expert, DEV), to_dev(r.x, DEV)
+    o = oracle.route_build(r.top_expert, E, m)
+    P = int(o["padded_bins"][-1])
+    o_xp = oracle.padded_gather(r.x, o["indices"], o["bin_ids"], o["bins"], o["padded_bins"], K)
+    side = torch.cuda.Stream(DEV)
+    st = status_word()
+    for _ in range(3):
+        side.wait_stream(torch.cuda.current_stream(DEV))
+        with torch.cuda.stream(side):
+            bxp = p.moe_padded_gather(bx, brt.indices, brt.bins, brt.padded_bins, big.K,
+                                      positions=brt.positions, status=st)
+            p.moe_padded_scatter(bxp, brt.indices, brt.bin_ids, brt.bins, brt.padded_bins, None, big.T, big.K,
+                                 positions=brt.positions, status=st)
+        route, xp = p.moe_route_build_padded_gather(te, x, E, m, status=st, one_launch=True)
+        torch.cuda.synchronize()
+        for k in ("indices", "bins", "padded_bins", "positions"):
+            assert_bits_equal(to_host(getattr(route, k)), o[k], "busy one-launch route.%s" % k)
+        assert_bits_equal(to_host(xp)[:P], o_xp, "busy one-launch padded gather")
+        assert int(st.item()) == 0
+
+
 def test_one_launch_bad_expert_ids_are_reported():
     E, K, T, H = 16, 2, 300, 64
     r = wl.uniform_routing("one-launch-bad", T, H, E, K, wl.BF16, capacity=50, pad_multiple=4, seed=3)

@@ -255,6 +255,9 @@ def test_fused_route_gather_tiny_and_edges(workspace):
     # more experts than threads of a CTA, many chunks per expert column
     run_fused(wl.zipf_routing("fused-e1000", 3000, 24, 1000, 6, wl.BF16, capacity=20, pad_multiple=8, seed=4),
               workspace=workspace)
+    # more experts than the bins the copy pass stages: the chained launches whatever the workspace
+    run_fused(wl.zipf_routing("fused-e1100", 2000, 24, 1100, 4, wl.BF16, capacity=20, pad_multiple=8, seed=5),
+              workspace=workspace)
 
 
 @pytest.mark.slow
